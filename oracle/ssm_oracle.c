@@ -1,0 +1,184 @@
+/*
+ * Plain fp64 CPU oracle for the selective state-space (S6) scan, its scalar-A
+ * multi-head (SSD) form and the single-token decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the test-suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header or constant with the
+ * CUDA library; the two meet only in the seeded input generators.
+ *
+ * Every routine is the sequential definition, one time step after another, in
+ * double precision, with no blocking, chunking or reordering:
+ *
+ *   - "Mamba 논문 리뷰: 선형 시간복잡도로 Transformer에 도전하는 Selective State
+ *     Space Model" (tildalice.io), section "Δ의 직관적 이해": the discretised
+ *     recurrence h_t = exp(Δ_t A) h_{t-1} + Δ_t B_t x_t (the simplified B̄ = ΔB),
+ *     section "Selection Mechanism": Δ_t = softplus(s_Δ(x_t)), and the
+ *     block diagram / reference class in section "Mamba 블록 아키텍처": readout
+ *     y_t = C_t h_t after the update, then the gate y·SiLU(z).
+ *   - "[yongggg's] Mamba: Linear-Time Sequence Modeling with Selective State
+ *     Spaces (Review)", section "State Space Model": the D skip term D·x.
+ *   - "Mamba-2: 상태 공간 기반 시퀀스 모델" (obsidian-dorae222.pages.dev),
+ *     sections "1-세미분리 행렬" and "멀티-헤드 구조": one independent SSM per
+ *     head with a scalar decay per head and B, C shared by the heads of a group.
+ *
+ * Readings where the pages are silent or garbled (all listed in the design
+ * notes): Δ is per channel; B̄ = ΔB; y = (C·h + D·x)·silu(z); the initial state
+ * is zero unless given; softplus(v) = log(1 + e^v) evaluated in the overflow-
+ * free form max(v,0) + log1p(exp(-|v|)).
+ *
+ * Layouts (row-major, last index fastest):
+ *   scan   : x, delta, z, y (B,L,D); Bm, Cm (B,L,N); A (D,N); Dv, bias (D);
+ *            h0, h_final (B,D,N)
+ *   ssd    : x, z, y (B,L,H,P); delta (B,L,H); A, Dv, bias (H);
+ *            Bm, Cm (B,L,G,N); h0, h_final (B,H,P,N)
+ *   decode : state (B,D,N) updated in place; x, delta, z, y (B,D); Bm, Cm (B,N);
+ *            A (D,N); Dv, bias (D)
+ * Nullable pointers: Dv, z, bias, h0, h_final (scan/ssd); Dv, z, bias (decode).
+ * Return value: 0 on success, -1 on a bad size, -2 on allocation failure.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* softplus(v) = log(1 + e^v), written so that neither branch overflows. */
+static double softplus_f64(double v)
+{
+    return (v > 0.0 ? v : 0.0) + log1p(exp(-fabs(v)));
+}
+
+/* SiLU(z) = z * sigmoid(z). */
+static double silu_f64(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+static double step_size(double raw, const double *bias, int64_t c, int softplus)
+{
+    double v = raw + (bias ? bias[c] : 0.0);
+    return softplus ? softplus_f64(v) : v;
+}
+
+int oracle_scan_f64(int64_t nb, int64_t L, int64_t D, int64_t N,
+                    const double *x, const double *delta, const double *A,
+                    const double *Bm, const double *Cm, const double *Dv,
+                    const double *z, const double *bias, int softplus,
+                    const double *h0, double *y, double *h_final, int nthreads)
+{
+    if (nb < 0 || L < 0 || D < 0 || N < 1) return -1;
+    int64_t chains = nb * D;
+    int failed = 0;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1) reduction(| : failed)
+    for (int64_t c = 0; c < chains; ++c) {
+        int64_t b = c / D, d = c % D;
+        double *h = (double *)malloc((size_t)N * sizeof(double));
+        if (!h) { failed |= 1; continue; }
+        for (int64_t n = 0; n < N; ++n) h[n] = h0 ? h0[(b * D + d) * N + n] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            int64_t bt = b * L + t;
+            double xv = x[bt * D + d];
+            double dl = step_size(delta[bt * D + d], bias, d, softplus);
+            /* state update: h <- exp(dl*A) h + dl*B_t*x_t */
+            for (int64_t n = 0; n < N; ++n)
+                h[n] = exp(dl * A[d * N + n]) * h[n] + dl * Bm[bt * N + n] * xv;
+            /* readout after the update, then the D skip and the gate */
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) acc += Cm[bt * N + n] * h[n];
+            double out = acc + (Dv ? Dv[d] : 0.0) * xv;
+            if (z) out *= silu_f64(z[bt * D + d]);
+            y[bt * D + d] = out;
+        }
+        if (h_final)
+            for (int64_t n = 0; n < N; ++n) h_final[(b * D + d) * N + n] = h[n];
+        free(h);
+    }
+    return failed ? -2 : 0;
+}
+
+int oracle_ssd_f64(int64_t nb, int64_t L, int64_t H, int64_t P, int64_t G, int64_t N,
+                   const double *x, const double *delta, const double *A,
+                   const double *Bm, const double *Cm, const double *Dv,
+                   const double *z, const double *bias, int softplus,
+                   const double *h0, double *y, double *h_final, int nthreads)
+{
+    if (nb < 0 || L < 0 || H < 1 || P < 1 || G < 1 || N < 1 || H % G) return -1;
+    int64_t heads_per_group = H / G;
+    int64_t chains = nb * H;
+    int failed = 0;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1) reduction(| : failed)
+    for (int64_t c = 0; c < chains; ++c) {
+        int64_t b = c / H, hd = c % H, g = hd / heads_per_group;
+        /* matrix state S (P x N) of head hd */
+        double *S = (double *)malloc((size_t)(P * N) * sizeof(double));
+        if (!S) { failed |= 1; continue; }
+        for (int64_t i = 0; i < P * N; ++i) S[i] = h0 ? h0[(b * H + hd) * P * N + i] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            int64_t bt = b * L + t;
+            double dl = step_size(delta[bt * H + hd], bias, hd, softplus);
+            double decay = exp(dl * A[hd]);
+            const double *Bt = Bm + (bt * G + g) * N;
+            const double *Ct = Cm + (bt * G + g) * N;
+            for (int64_t p = 0; p < P; ++p) {
+                double xv = x[(bt * H + hd) * P + p];
+                double *Sp = S + p * N;
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    Sp[n] = decay * Sp[n] + dl * xv * Bt[n];
+                    acc += Ct[n] * Sp[n];
+                }
+                double out = acc + (Dv ? Dv[hd] : 0.0) * xv;
+                if (z) out *= silu_f64(z[(bt * H + hd) * P + p]);
+                y[(bt * H + hd) * P + p] = out;
+            }
+        }
+        if (h_final)
+            for (int64_t i = 0; i < P * N; ++i) h_final[(b * H + hd) * P * N + i] = S[i];
+        free(S);
+    }
+    return failed ? -2 : 0;
+}
+
+int oracle_decode_f64(int64_t nb, int64_t D, int64_t N, double *state,
+                      const double *x, const double *delta, const double *A,
+                      const double *Bm, const double *Cm, const double *Dv,
+                      const double *z, const double *bias, int softplus,
+                      double *y, int nthreads)
+{
+    if (nb < 0 || D < 0 || N < 1) return -1;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int64_t c = 0; c < nb * D; ++c) {
+        int64_t b = c / D, d = c % D;
+        double xv = x[c];
+        double dl = step_size(delta[c], bias, d, softplus);
+        double *h = state + c * N;
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            h[n] = exp(dl * A[d * N + n]) * h[n] + dl * Bm[b * N + n] * xv;
+            acc += Cm[b * N + n] * h[n];
+        }
+        double out = acc + (Dv ? Dv[d] : 0.0) * xv;
+        if (z) out *= silu_f64(z[c]);
+        y[c] = out;
+    }
+    return 0;
+}
+
+/* Helper exposed for the pins: the scalar softplus used above. */
+double oracle_softplus_f64(double v) { return softplus_f64(v); }
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
