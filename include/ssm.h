@@ -1,0 +1,161 @@
+/*
+ * ssm.h — C ABI of the B300 selective state-space library (libssm.so).
+ *
+ * Three operations, all forward, all on one GPU:
+ *
+ *   ssm_scan_fwd      the selective (S6) scan.  Per channel d of batch b:
+ *                       dl_t  = softplus(delta_t + bias_d)      (or without softplus)
+ *                       h_t   = exp(dl_t * A_d) (.) h_{t-1} + dl_t * B_t * x_t
+ *                       y_t   = (C_t . h_t + D_d * x_t) * silu(z_t)   (gate optional)
+ *                     Defined by "Mamba 논문 리뷰: 선형 시간복잡도로 Transformer에
+ *                     도전하는 Selective State Space Model" (tildalice.io), sections
+ *                     "Selection Mechanism" (Δ_t = softplus(s_Δ(x_t))), "Δ의 직관적
+ *                     이해" (the recurrence with B̄ = ΔB) and "Mamba 블록 아키텍처"
+ *                     (the SiLU gate); the D skip term from "[yongggg's] Mamba ...
+ *                     (Review)", section "State Space Model".
+ *
+ *   ssm_ssd_chunk_fwd the same recurrence with a scalar decay per head and a P x N
+ *                     matrix state per head (Mamba-2), computed in its chunked dual
+ *                     form: inside a chunk Y = (L o C B^T)(dl x), between chunks the
+ *                     state is passed on.  "Mamba-2: 상태 공간 기반 시퀀스 모델"
+ *                     (obsidian-dorae222.pages.dev), sections "1-세미분리 행렬",
+ *                     "SSM-Attention 동치성", "멀티-헤드 구조" and "SSD 타일링 알고리즘".
+ *
+ *   ssm_step_decode   one recurrent step for one new token per sequence, updating a
+ *                     fixed-size state in place (tildalice review, section "추론 속도":
+ *                     O(D x N) state, no cache that grows with the sequence).
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer to a dense row-major array; the caller
+ *     allocates and owns all of them, the workspace included.  The library never
+ *     allocates or frees memory and keeps no per-call state.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).  They
+ *     validate their arguments on the host first and, on any error, return a status
+ *     without launching anything.
+ *   - I/O dtype: x, delta, B, C, z and y are all `io_dtype` (fp32 or bf16).  A, D,
+ *     delta_bias, the states and every intermediate are fp32.  bf16 outputs are
+ *     rounded once, to nearest even.
+ *   - y must not alias any input.  The decode state is updated in place by design.
+ *   - Errors found on the device (a bounded wait that ran out) are written to a
+ *     status word at the start of the workspace; read it with ssm_read_device_status.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef SSM_B300_H
+#define SSM_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t. */
+typedef struct CUstream_st *ssm_stream_t;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1, /* a null required pointer, a negative size, H % G != 0, ... */
+    SSM_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement (e.g. N > 64) */
+    SSM_ERR_ALIGNMENT = 3,   /* a pointer is not aligned to its element size */
+    SSM_ERR_WORKSPACE = 4,   /* workspace missing or smaller than *_workspace_size says */
+    SSM_ERR_CUDA = 5,        /* the CUDA runtime reported an error at launch */
+    SSM_ERR_TIMEOUT = 6      /* (device status only) a bounded wait gave up */
+} ssm_status;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/* ------------------------------------------------------------------ S6 scan
+ * Shapes (B = batch, L = seqlen, D = dim, N = dstate):
+ *   x, delta, z, y : (B, L, D) io_dtype        B, C : (B, L, N) io_dtype
+ *   A              : (D, N) fp32 (expected < 0) D, delta_bias : (D) fp32
+ *   h0, h_final    : (B, D, N) fp32
+ * Nullable: D (no skip), delta_bias (zero), z (no gate), h0 (zero initial state),
+ * h_final (final state not returned).  Sizes: B, L >= 0, D >= 1, 1 <= N <= 64.
+ * B, L or D of zero is valid; then only h_final (= h0, or zeros) is written.
+ * time_chunk: 0 lets the library choose how many time steps one thread block walks;
+ * a positive value (a multiple of 32) forces it, which splits long sequences over
+ * several blocks joined by a carry pass (exact up to rounding).
+ * Workspace: ssm_scan_workspace_size() bytes (it reads only the sizes and flags of
+ * `args`, not the pointers; 0 means none is needed), 256-byte aligned; contents
+ * need no initialisation. */
+typedef struct {
+    int64_t batch, seqlen, dim, dstate;
+    int64_t time_chunk;
+    int32_t io_dtype;       /* ssm_dtype */
+    int32_t delta_softplus; /* 0 or 1 */
+    const void *x, *delta, *B, *C, *z;
+    const float *A, *D, *delta_bias, *h0;
+    void *y;
+    float *h_final;
+    void *workspace;
+    size_t workspace_bytes;
+} ssm_scan_args;
+
+SSM_API ssm_status ssm_scan_workspace_size(const ssm_scan_args *args, size_t *bytes);
+SSM_API ssm_status ssm_scan_fwd(const ssm_scan_args *args, ssm_stream_t stream);
+
+/* ------------------------------------------------------------------ SSD (Mamba-2)
+ * Shapes (H = nheads, P = headdim, G = ngroups, N = dstate; head h reads group
+ * h / (H / G)):
+ *   x, z, y : (B, L, H, P) io_dtype     delta : (B, L, H) io_dtype
+ *   B, C    : (B, L, G, N) io_dtype     A, D, delta_bias : (H) fp32
+ *   h0, h_final : (B, H, P, N) fp32
+ * Nullable: D, delta_bias, z, h0, h_final.  H % G == 0.  chunk_size: the chunk
+ * length Q of the dual form (0 = 256); the result does not depend on it beyond
+ * rounding.  Workspace: ssm_ssd_workspace_size() bytes, 256-byte aligned. */
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, ngroups, dstate;
+    int64_t chunk_size;
+    int32_t io_dtype;
+    int32_t delta_softplus;
+    const void *x, *delta, *B, *C, *z;
+    const float *A, *D, *delta_bias, *h0;
+    void *y;
+    float *h_final;
+    void *workspace;
+    size_t workspace_bytes;
+} ssm_ssd_args;
+
+SSM_API ssm_status ssm_ssd_workspace_size(const ssm_ssd_args *args, size_t *bytes);
+SSM_API ssm_status ssm_ssd_chunk_fwd(const ssm_ssd_args *args, ssm_stream_t stream);
+
+/* ------------------------------------------------------------------ decode step
+ * Shapes: state (B, D, N) fp32, read and written IN PLACE;
+ *   x, delta, z, y : (B, D) io_dtype    B, C : (B, N) io_dtype
+ *   A : (D, N) fp32                    D, delta_bias : (D) fp32
+ * Nullable: D, delta_bias, z.  One call advances every sequence by one token;
+ * calls on one stream are ordered, so L calls equal one ssm_scan_fwd over L steps
+ * (up to rounding).  No workspace. */
+typedef struct {
+    int64_t batch, dim, dstate;
+    int32_t io_dtype;
+    int32_t delta_softplus;
+    float *state;
+    const void *x, *delta, *B, *C, *z;
+    const float *A, *D, *delta_bias;
+    void *y;
+} ssm_decode_args;
+
+SSM_API ssm_status ssm_step_decode(const ssm_decode_args *args, ssm_stream_t stream);
+
+/* ------------------------------------------------------------------ utilities */
+SSM_API const char *ssm_status_string(ssm_status status);
+SSM_API int ssm_version(void); /* major * 10000 + minor * 100 + patch */
+
+/* Synchronises `stream`, then reads the device status word that the kernels of
+ * the last call using `workspace` left there (SSM_OK when none failed). */
+SSM_API ssm_status ssm_read_device_status(const void *workspace, ssm_stream_t stream,
+                                  ssm_status *device_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_B300_H */

@@ -1,0 +1,21 @@
+"""B300-native selective state-space (S6) scan, SSD chunk form and decode step.
+
+The compute lives in ``libssm.so`` (hand-written CUDA for sm_103a, C ABI in
+``include/ssm.h``).  This module is a thin ctypes binding: it checks tensor
+dtypes and shapes, allocates outputs and workspaces with PyTorch, and passes raw
+device pointers and the current CUDA stream.  Every step of the computation runs
+in the library's kernels; if the library is missing, the calls raise.
+
+    y, h_final = scan_fwd(x, delta, A, B, C, D=..., z=..., delta_bias=...)
+    y, h_final = ssd_chunk_fwd(x, delta, A, B, C, D=..., chunk_size=256)
+    y          = step_decode(state, x, delta, A, B, C, D=..., z=...)  # state in place
+"""
+from __future__ import annotations
+
+from .binding import (SSMError, build_library, library_path, load_library, scan_fwd,
+                      scan_workspace_size, ssd_chunk_fwd, ssd_workspace_size, step_decode,
+                      version)
+
+__all__ = ["SSMError", "build_library", "library_path", "load_library", "scan_fwd",
+           "scan_workspace_size", "ssd_chunk_fwd", "ssd_workspace_size", "step_decode",
+           "version"]

@@ -1,0 +1,309 @@
+"""ctypes binding of libssm.so (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libssm.so")
+_lib = None
+
+SSM_F32, SSM_BF16 = 0, 1
+_STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED",
+           3: "SSM_ERR_ALIGNMENT", 4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA",
+           6: "SSM_ERR_TIMEOUT"}
+
+EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_ssd_workspace_size",
+            "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_status_string", "ssm_version",
+            "ssm_read_device_status"]
+
+_i64, _i32, _vp, _fp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p
+
+
+class ScanArgs(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("seqlen", _i64), ("dim", _i64), ("dstate", _i64),
+                ("time_chunk", _i64), ("io_dtype", _i32), ("delta_softplus", _i32),
+                ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp), ("z", _vp),
+                ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("h0", _fp),
+                ("y", _vp), ("h_final", _fp), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class SSDArgs(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("seqlen", _i64), ("nheads", _i64), ("headdim", _i64),
+                ("ngroups", _i64), ("dstate", _i64), ("chunk_size", _i64),
+                ("io_dtype", _i32), ("delta_softplus", _i32),
+                ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp), ("z", _vp),
+                ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("h0", _fp),
+                ("y", _vp), ("h_final", _fp), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("dim", _i64), ("dstate", _i64),
+                ("io_dtype", _i32), ("delta_softplus", _i32), ("state", _fp),
+                ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp), ("z", _vp),
+                ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("y", _vp)]
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _STATUS.get(status, str(status))
+        try:
+            msg += ": " + load_library().ssm_status_string(status).decode()
+        except Exception:
+            pass
+        super().__init__(f"{where} failed with {msg}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def build_library(force: bool = False) -> str:
+    from .build import build
+    return build(force=force)
+
+
+def load_library():
+    """Load libssm.so from the package directory (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                           "`python -m selective_state_space_132_b300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    lib.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanArgs),
+                                            ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanArgs), _vp]
+    lib.ssm_ssd_workspace_size.argtypes = [ctypes.POINTER(SSDArgs),
+                                           ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssm_ssd_chunk_fwd.argtypes = [ctypes.POINTER(SSDArgs), _vp]
+    lib.ssm_step_decode.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+    lib.ssm_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
+    for fn in ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_ssd_workspace_size",
+               "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_read_device_status"):
+        getattr(lib, fn).restype = ctypes.c_int
+    lib.ssm_status_string.argtypes = [ctypes.c_int]
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def version() -> int:
+    return int(load_library().ssm_version())
+
+
+# ---------------------------------------------------------------- helpers
+def _io_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    if t.dtype == torch.float32:
+        return SSM_F32
+    raise TypeError(f"I/O tensors must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _check(t: Optional[torch.Tensor], name: str, shape, dtype, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _raise(rc: int, where: str):
+    if rc != 0:
+        raise SSMError(rc, where)
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace of {workspace.numel()} bytes < {nbytes} needed")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+# ---------------------------------------------------------------- scan
+def _scan_args(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final,
+               time_chunk) -> ScanArgs:
+    nb, L, Dm = x.shape
+    N = A.shape[1]
+    dev, io = x.device, x.dtype
+    _io_code(x)
+    _check(delta, "delta", (nb, L, Dm), io, dev)
+    _check(A, "A", (Dm, N), torch.float32, dev)
+    _check(B, "B", (nb, L, N), io, dev)
+    _check(C, "C", (nb, L, N), io, dev)
+    _check(D, "D", (Dm,), torch.float32, dev)
+    _check(z, "z", (nb, L, Dm), io, dev)
+    _check(delta_bias, "delta_bias", (Dm,), torch.float32, dev)
+    _check(h0, "h0", (nb, Dm, N), torch.float32, dev)
+    _check(y, "y", (nb, L, Dm), io, dev)
+    _check(h_final, "h_final", (nb, Dm, N), torch.float32, dev)
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    return ScanArgs(nb, L, Dm, N, int(time_chunk), _io_code(x), int(bool(delta_softplus)),
+                    _ptr(x), _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
+                    _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(h_final), None, 0)
+
+
+def scan_workspace_size(batch: int, seqlen: int, dim: int, dstate: int,
+                        io_dtype=torch.bfloat16, time_chunk: int = 0) -> int:
+    a = ScanArgs(batch, seqlen, dim, dstate, int(time_chunk),
+                 SSM_BF16 if io_dtype == torch.bfloat16 else SSM_F32, 1,
+                 1024, 1024, 1024, 1024, None, 1024, None, None, None, 4096, None, None, 0)
+    out = ctypes.c_size_t(0)
+    _raise(load_library().ssm_scan_workspace_size(ctypes.byref(a), ctypes.byref(out)),
+           "ssm_scan_workspace_size")
+    return int(out.value)
+
+
+def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+             C: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+             delta_bias: Optional[torch.Tensor] = None, delta_softplus: bool = True,
+             h0: Optional[torch.Tensor] = None, return_final_state: bool = True,
+             y: Optional[torch.Tensor] = None, h_final: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, time_chunk: int = 0,
+             stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Selective scan.  x, delta, z: (B, L, D); A: (D, N) fp32; B, C: (B, L, N);
+    D, delta_bias: (D,) fp32; h0: (B, D, N) fp32.  Returns (y, h_final)."""
+    lib = load_library()
+    nb, L, Dm = x.shape
+    N = A.shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    if h_final is None and return_final_state:
+        h_final = torch.empty((nb, Dm, N), dtype=torch.float32, device=x.device)
+    args = _scan_args(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final,
+                      time_chunk)
+    need = ctypes.c_size_t(0)
+    _raise(lib.ssm_scan_workspace_size(ctypes.byref(args), ctypes.byref(need)),
+           "ssm_scan_workspace_size")
+    ws, nbytes = _workspace(int(need.value), x.device, workspace)
+    args.workspace, args.workspace_bytes = _ptr(ws), nbytes
+    _raise(lib.ssm_scan_fwd(ctypes.byref(args), _stream(stream)), "ssm_scan_fwd")
+    return y, h_final
+
+
+# ---------------------------------------------------------------- SSD
+def _ssd_args(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final,
+              chunk_size) -> SSDArgs:
+    nb, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev, io = x.device, x.dtype
+    _io_code(x)
+    _check(delta, "delta", (nb, L, H), io, dev)
+    _check(A, "A", (H,), torch.float32, dev)
+    _check(B, "B", (nb, L, G, N), io, dev)
+    _check(C, "C", (nb, L, G, N), io, dev)
+    _check(D, "D", (H,), torch.float32, dev)
+    _check(z, "z", (nb, L, H, P), io, dev)
+    _check(delta_bias, "delta_bias", (H,), torch.float32, dev)
+    _check(h0, "h0", (nb, H, P, N), torch.float32, dev)
+    _check(y, "y", (nb, L, H, P), io, dev)
+    _check(h_final, "h_final", (nb, H, P, N), torch.float32, dev)
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    return SSDArgs(nb, L, H, P, G, N, int(chunk_size), _io_code(x), int(bool(delta_softplus)),
+                   _ptr(x), _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
+                   _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(h_final), None, 0)
+
+
+def ssd_workspace_size(x, delta, A, B, C, chunk_size: int = 256) -> int:
+    args = _ssd_args(x, delta, A, B, C, None, None, None, True, None, None, None, chunk_size)
+    out = ctypes.c_size_t(0)
+    _raise(load_library().ssm_ssd_workspace_size(ctypes.byref(args), ctypes.byref(out)),
+           "ssm_ssd_workspace_size")
+    return int(out.value)
+
+
+def ssd_chunk_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                  C: torch.Tensor, D: Optional[torch.Tensor] = None,
+                  z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
+                  delta_softplus: bool = True, h0: Optional[torch.Tensor] = None,
+                  chunk_size: int = 256, return_final_state: bool = True,
+                  y: Optional[torch.Tensor] = None, h_final: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None,
+                  stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Multi-head scalar-A SSM (Mamba-2 SSD).  x, z: (B, L, H, P); delta: (B, L, H);
+    A, D, delta_bias: (H,) fp32; B, C: (B, L, G, N); h0: (B, H, P, N) fp32."""
+    lib = load_library()
+    nb, L, H, P = x.shape
+    N = B.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    if h_final is None and return_final_state:
+        h_final = torch.empty((nb, H, P, N), dtype=torch.float32, device=x.device)
+    args = _ssd_args(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final,
+                     chunk_size)
+    need = ctypes.c_size_t(0)
+    _raise(lib.ssm_ssd_workspace_size(ctypes.byref(args), ctypes.byref(need)),
+           "ssm_ssd_workspace_size")
+    ws, nbytes = _workspace(int(need.value), x.device, workspace)
+    args.workspace, args.workspace_bytes = _ptr(ws), nbytes
+    _raise(lib.ssm_ssd_chunk_fwd(ctypes.byref(args), _stream(stream)), "ssm_ssd_chunk_fwd")
+    return y, h_final
+
+
+def read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    out = ctypes.c_int(0)
+    _raise(load_library().ssm_read_device_status(_ptr(workspace), _stream(stream),
+                                                 ctypes.byref(out)), "ssm_read_device_status")
+    return int(out.value)
+
+
+# ---------------------------------------------------------------- decode
+def step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor,
+                B: torch.Tensor, C: torch.Tensor, D: Optional[torch.Tensor] = None,
+                z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
+                delta_softplus: bool = True, y: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """One recurrent step; ``state`` (B, D, N) fp32 is updated in place.
+    x, delta, z: (B, D); B, C: (B, N); A: (D, N) fp32; D, delta_bias: (D,) fp32."""
+    lib = load_library()
+    nb, Dm, N = state.shape
+    dev, io = x.device, x.dtype
+    _io_code(x)
+    _check(state, "state", (nb, Dm, N), torch.float32, dev)
+    _check(x, "x", (nb, Dm), io, dev)
+    _check(delta, "delta", (nb, Dm), io, dev)
+    _check(A, "A", (Dm, N), torch.float32, dev)
+    _check(B, "B", (nb, N), io, dev)
+    _check(C, "C", (nb, N), io, dev)
+    _check(D, "D", (Dm,), torch.float32, dev)
+    _check(z, "z", (nb, Dm), io, dev)
+    _check(delta_bias, "delta_bias", (Dm,), torch.float32, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    _check(y, "y", (nb, Dm), io, dev)
+    args = DecodeArgs(nb, Dm, N, _io_code(x), int(bool(delta_softplus)), _ptr(state), _ptr(x),
+                      _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
+                      _ptr(delta_bias), _ptr(y))
+    _raise(lib.ssm_step_decode(ctypes.byref(args), _stream(stream)), "ssm_step_decode")
+    return y

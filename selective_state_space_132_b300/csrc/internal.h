@@ -1,0 +1,59 @@
+// Launch interfaces between the C ABI layer (ssm_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssm {
+
+struct ScanParams {
+    int64_t batch, seqlen, dim, dstate;
+    int io_bf16;        // 1: bf16 I/O, fast math; 0: fp32 I/O, accurate math
+    int softplus;
+    const void *x, *delta, *Bm, *Cm, *z;
+    const float *A, *Dv, *bias, *h0;
+    void *y;
+    float *h_final;
+    // carry across time chunks (workspace)
+    int64_t chunk_len;  // steps per time chunk (multiple of the time tile)
+    int nchunks;        // K
+    float *hloc;        // (B, K, D, N) local end states of chunks 0..K-2
+    float *dsum;        // (B, K, D) sum of steps of chunks 0..K-2
+    bool vec_ok;        // 16-byte vector loads allowed
+};
+
+// Number of time chunks and chunk length the scan uses for these sizes.
+void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t time_chunk,
+               int64_t *chunk_len, int *nchunks);
+size_t scan_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, int nchunks);
+cudaError_t launch_scan(const ScanParams &p, cudaStream_t stream);
+
+struct DecodeParams {
+    int64_t batch, dim, dstate;
+    int io_bf16;
+    int softplus;
+    float *state;
+    const void *x, *delta, *Bm, *Cm, *z;
+    const float *A, *Dv, *bias;
+    void *y;
+};
+cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
+
+struct SSDParams {
+    int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk;
+    int io_bf16;
+    int softplus;
+    const void *x, *delta, *Bm, *Cm, *z;
+    const float *A, *Dv, *bias, *h0;
+    void *y;
+    float *h_final;
+    void *status;  // DeviceStatus at the start of the workspace
+    void *work;    // rest of the workspace
+    size_t work_bytes;
+};
+size_t ssd_workspace_bytes(const SSDParams &p);
+cudaError_t launch_ssd(const SSDParams &p, cudaStream_t stream);
+cudaError_t launch_ssd_recurrent(const SSDParams &p, cudaStream_t stream);
+
+}  // namespace ssm

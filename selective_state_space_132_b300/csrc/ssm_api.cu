@@ -1,0 +1,283 @@
+// C ABI of libssm.so: host-side validation, workspace sizing and dispatch to the
+// kernels.  Every check runs before any launch; on failure nothing is enqueued.
+#include "../../include/ssm.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+using ssm::kStatusBytes;
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t io_size(int32_t dt) { return dt == SSM_BF16 ? 2 : 4; }
+
+// [p, p + bytes) overlaps [q, q + qbytes)
+bool overlaps(const void *p, size_t bytes, const void *q, size_t qbytes) {
+    if (!p || !q || bytes == 0 || qbytes == 0) return false;
+    auto a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + qbytes && b < a + bytes;
+}
+
+ssm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA; }
+
+// ------------------------------------------------------------------ scan
+ssm_status check_scan(const ssm_scan_args *a, bool pointers = true) {
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->batch < 0 || a->seqlen < 0 || a->dim < 0 || a->dstate < 1) return SSM_ERR_INVALID_ARG;
+    if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (a->delta_softplus != 0 && a->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (a->time_chunk < 0 || a->time_chunk % 32 != 0) return SSM_ERR_INVALID_ARG;
+    if (a->dstate > 64) return SSM_ERR_UNSUPPORTED;
+    if (a->batch > 65535) return SSM_ERR_UNSUPPORTED;
+    if (a->seqlen > (int64_t)1 << 40 || a->dim > (int64_t)1 << 31) return SSM_ERR_UNSUPPORTED;
+    if (!pointers) return SSM_OK;
+    const bool tokens = a->batch * a->seqlen * a->dim > 0;
+    const bool rows = a->batch * a->seqlen > 0;
+    if (tokens && (!a->x || !a->delta || !a->y)) return SSM_ERR_INVALID_ARG;
+    if (rows && a->dim > 0 && (!a->B || !a->C)) return SSM_ERR_INVALID_ARG;
+    if (a->dim > 0 && !a->A) return SSM_ERR_INVALID_ARG;
+    const size_t e = io_size(a->io_dtype);
+    const void *io_ptrs[] = {a->x, a->delta, a->B, a->C, a->z, a->y};
+    for (const void *p : io_ptrs)
+        if (!aligned(p, e)) return SSM_ERR_ALIGNMENT;
+    const void *f_ptrs[] = {a->A, a->D, a->delta_bias, a->h0, a->h_final};
+    for (const void *p : f_ptrs)
+        if (!aligned(p, 4)) return SSM_ERR_ALIGNMENT;
+    const size_t tok_bytes = (size_t)(a->batch * a->seqlen * a->dim) * e;
+    const size_t bc_bytes = (size_t)(a->batch * a->seqlen * a->dstate) * e;
+    const size_t st_bytes = (size_t)(a->batch * a->dim * a->dstate) * 4;
+    if (overlaps(a->y, tok_bytes, a->x, tok_bytes) || overlaps(a->y, tok_bytes, a->delta, tok_bytes) ||
+        overlaps(a->y, tok_bytes, a->z, tok_bytes) || overlaps(a->y, tok_bytes, a->B, bc_bytes) ||
+        overlaps(a->y, tok_bytes, a->C, bc_bytes) || overlaps(a->h_final, st_bytes, a->h0, st_bytes) ||
+        overlaps(a->y, tok_bytes, a->h_final, st_bytes))
+        return SSM_ERR_INVALID_ARG;
+    return SSM_OK;
+}
+
+size_t scan_ws(const ssm_scan_args *a, int64_t *chunk_len, int *nchunks) {
+    ssm::scan_plan(a->batch, a->seqlen, a->dim, a->dstate, a->time_chunk, chunk_len, nchunks);
+    if (*nchunks <= 1) return 0;
+    return ssm::scan_workspace_bytes(a->batch, a->dim, a->dstate, *nchunks);
+}
+
+// ------------------------------------------------------------------ ssd
+ssm_status check_ssd(const ssm_ssd_args *a, bool pointers = true) {
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->batch < 0 || a->seqlen < 0 || a->nheads < 1 || a->headdim < 1 || a->ngroups < 1 ||
+        a->dstate < 1 || a->chunk_size < 0)
+        return SSM_ERR_INVALID_ARG;
+    if (a->nheads % a->ngroups != 0) return SSM_ERR_INVALID_ARG;
+    if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (a->delta_softplus != 0 && a->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (a->dstate > 256) return SSM_ERR_UNSUPPORTED;
+    if (a->batch * a->nheads * a->headdim > ((int64_t)1 << 31)) return SSM_ERR_UNSUPPORTED;
+    if (!pointers) return SSM_OK;
+    const bool rows = a->batch * a->seqlen > 0;
+    if (rows && (!a->x || !a->delta || !a->y || !a->B || !a->C)) return SSM_ERR_INVALID_ARG;
+    if (!a->A) return SSM_ERR_INVALID_ARG;
+    const size_t e = io_size(a->io_dtype);
+    const void *io_ptrs[] = {a->x, a->delta, a->B, a->C, a->z, a->y};
+    for (const void *p : io_ptrs)
+        if (!aligned(p, e)) return SSM_ERR_ALIGNMENT;
+    const void *f_ptrs[] = {a->A, a->D, a->delta_bias, a->h0, a->h_final};
+    for (const void *p : f_ptrs)
+        if (!aligned(p, 4)) return SSM_ERR_ALIGNMENT;
+    if (a->workspace && !aligned(a->workspace, 256)) return SSM_ERR_ALIGNMENT;
+    const size_t tok = (size_t)(a->batch * a->seqlen * a->nheads * a->headdim) * e;
+    const size_t bc = (size_t)(a->batch * a->seqlen * a->ngroups * a->dstate) * e;
+    const size_t dl = (size_t)(a->batch * a->seqlen * a->nheads) * e;
+    const size_t st = (size_t)(a->batch * a->nheads * a->headdim * a->dstate) * 4;
+    if (overlaps(a->y, tok, a->x, tok) || overlaps(a->y, tok, a->z, tok) ||
+        overlaps(a->y, tok, a->B, bc) || overlaps(a->y, tok, a->C, bc) ||
+        overlaps(a->y, tok, a->delta, dl) || overlaps(a->h_final, st, a->h0, st) ||
+        overlaps(a->y, tok, a->h_final, st))
+        return SSM_ERR_INVALID_ARG;
+    return SSM_OK;
+}
+
+ssm::SSDParams ssd_params(const ssm_ssd_args *a) {
+    ssm::SSDParams p{};
+    p.batch = a->batch;
+    p.seqlen = a->seqlen;
+    p.nheads = a->nheads;
+    p.headdim = a->headdim;
+    p.ngroups = a->ngroups;
+    p.dstate = a->dstate;
+    p.chunk = a->chunk_size > 0 ? a->chunk_size : 256;
+    p.io_bf16 = a->io_dtype == SSM_BF16;
+    p.softplus = a->delta_softplus;
+    p.x = a->x;
+    p.delta = a->delta;
+    p.Bm = a->B;
+    p.Cm = a->C;
+    p.z = a->z;
+    p.A = a->A;
+    p.Dv = a->D;
+    p.bias = a->delta_bias;
+    p.h0 = a->h0;
+    p.y = a->y;
+    p.h_final = a->h_final;
+    p.status = a->workspace;
+    p.work = a->workspace ? static_cast<char *>(a->workspace) + kStatusBytes : nullptr;
+    p.work_bytes = a->workspace_bytes > kStatusBytes ? a->workspace_bytes - kStatusBytes : 0;
+    return p;
+}
+
+// ------------------------------------------------------------------ decode
+ssm_status check_decode(const ssm_decode_args *a) {
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->batch < 0 || a->dim < 0 || a->dstate < 1) return SSM_ERR_INVALID_ARG;
+    if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (a->delta_softplus != 0 && a->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (a->dstate > 64) return SSM_ERR_UNSUPPORTED;
+    if (a->batch * a->dim * 16 > ((int64_t)1 << 40)) return SSM_ERR_UNSUPPORTED;
+    if (a->batch * a->dim > 0 &&
+        (!a->state || !a->x || !a->delta || !a->B || !a->C || !a->A || !a->y))
+        return SSM_ERR_INVALID_ARG;
+    const size_t e = io_size(a->io_dtype);
+    const void *io_ptrs[] = {a->x, a->delta, a->B, a->C, a->z, a->y};
+    for (const void *p : io_ptrs)
+        if (!aligned(p, e)) return SSM_ERR_ALIGNMENT;
+    const void *f_ptrs[] = {a->state, a->A, a->D, a->delta_bias};
+    for (const void *p : f_ptrs)
+        if (!aligned(p, 4)) return SSM_ERR_ALIGNMENT;
+    const size_t tok = (size_t)(a->batch * a->dim) * e;
+    const size_t st = (size_t)(a->batch * a->dim * a->dstate) * 4;
+    if (overlaps(a->y, tok, a->x, tok) || overlaps(a->y, tok, a->delta, tok) ||
+        overlaps(a->y, tok, a->z, tok) || overlaps(a->y, tok, a->state, st))
+        return SSM_ERR_INVALID_ARG;
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ssm_status_string(ssm_status s) {
+    switch (s) {
+        case SSM_OK: return "ok";
+        case SSM_ERR_INVALID_ARG: return "invalid argument";
+        case SSM_ERR_UNSUPPORTED: return "unsupported size or configuration";
+        case SSM_ERR_ALIGNMENT: return "misaligned pointer";
+        case SSM_ERR_WORKSPACE: return "workspace missing or too small";
+        case SSM_ERR_CUDA: return "CUDA runtime error";
+        case SSM_ERR_TIMEOUT: return "a bounded device wait timed out";
+    }
+    return "unknown status";
+}
+
+int ssm_version(void) { return kVersion; }
+
+ssm_status ssm_scan_workspace_size(const ssm_scan_args *a, size_t *bytes) {
+    if (!bytes) return SSM_ERR_INVALID_ARG;
+    ssm_status s = check_scan(a, false);
+    if (s != SSM_OK) return s;
+    int64_t cl;
+    int k;
+    *bytes = scan_ws(a, &cl, &k);
+    return SSM_OK;
+}
+
+ssm_status ssm_scan_fwd(const ssm_scan_args *a, ssm_stream_t stream) {
+    ssm_status s = check_scan(a);
+    if (s != SSM_OK) return s;
+    int64_t cl;
+    int k;
+    const size_t need = scan_ws(a, &cl, &k);
+    if (need > 0 && (!a->workspace || a->workspace_bytes < need)) return SSM_ERR_WORKSPACE;
+    if (need > 0 && !aligned(a->workspace, 256)) return SSM_ERR_ALIGNMENT;
+    if (a->batch == 0 || a->dim == 0) return SSM_OK;  // nothing to write
+    ssm::ScanParams p{};
+    p.batch = a->batch;
+    p.seqlen = a->seqlen;
+    p.dim = a->dim;
+    p.dstate = a->dstate;
+    p.io_bf16 = a->io_dtype == SSM_BF16;
+    p.softplus = a->delta_softplus;
+    p.x = a->x;
+    p.delta = a->delta;
+    p.Bm = a->B;
+    p.Cm = a->C;
+    p.z = a->z;
+    p.A = a->A;
+    p.Dv = a->D;
+    p.bias = a->delta_bias;
+    p.h0 = a->h0;
+    p.y = a->y;
+    p.h_final = a->h_final;
+    p.chunk_len = cl;
+    p.nchunks = k;
+    if (k > 1) {
+        char *ws = static_cast<char *>(a->workspace) + kStatusBytes;
+        const size_t rows = (size_t)a->batch * k * a->dim;
+        p.hloc = reinterpret_cast<float *>(ws);
+        p.dsum = reinterpret_cast<float *>(ws + (rows * a->dstate * sizeof(float) + 255) / 256 * 256);
+    }
+    return from_cuda(ssm::launch_scan(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ssm_status ssm_ssd_workspace_size(const ssm_ssd_args *a, size_t *bytes) {
+    if (!bytes) return SSM_ERR_INVALID_ARG;
+    ssm_status s = check_ssd(a, false);
+    if (s != SSM_OK) return s;
+    *bytes = ssm::ssd_workspace_bytes(ssd_params(a));
+    return SSM_OK;
+}
+
+ssm_status ssm_ssd_chunk_fwd(const ssm_ssd_args *a, ssm_stream_t stream) {
+    ssm_status s = check_ssd(a);
+    if (s != SSM_OK) return s;
+    ssm::SSDParams p = ssd_params(a);
+    const size_t need = ssm::ssd_workspace_bytes(p);
+    if (!a->workspace || a->workspace_bytes < need) return SSM_ERR_WORKSPACE;
+    if (a->batch == 0) return SSM_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(a->workspace, 0, kStatusBytes, st);
+    if (e != cudaSuccess) return SSM_ERR_CUDA;
+    return from_cuda(ssm::launch_ssd(p, st));
+}
+
+ssm_status ssm_step_decode(const ssm_decode_args *a, ssm_stream_t stream) {
+    ssm_status s = check_decode(a);
+    if (s != SSM_OK) return s;
+    if (a->batch * a->dim == 0) return SSM_OK;
+    ssm::DecodeParams p{};
+    p.batch = a->batch;
+    p.dim = a->dim;
+    p.dstate = a->dstate;
+    p.io_bf16 = a->io_dtype == SSM_BF16;
+    p.softplus = a->delta_softplus;
+    p.state = a->state;
+    p.x = a->x;
+    p.delta = a->delta;
+    p.Bm = a->B;
+    p.Cm = a->C;
+    p.z = a->z;
+    p.A = a->A;
+    p.Dv = a->D;
+    p.bias = a->delta_bias;
+    p.y = a->y;
+    return from_cuda(ssm::launch_decode(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ssm_status ssm_read_device_status(const void *workspace, ssm_stream_t stream,
+                                  ssm_status *device_status) {
+    if (!workspace || !device_status) return SSM_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SSM_ERR_CUDA;
+    int32_t code = 0;
+    if (cudaMemcpy(&code, workspace, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    *device_status = static_cast<ssm_status>(code);
+    return SSM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+// One recurrent decode step (tildalice.io Mamba review, section "추론 속도": the
+// state has a fixed O(D x N) size and no cache grows with the sequence).  For
+// every sequence b and channel d, with one new token:
+//   dl = softplus(delta + bias_d)
+//   h  = exp(dl A_d) (.) h + (dl x) B          (state read and written in place)
+//   y  = (C . h + D_d x) * silu(z)
+//
+// B300 mapping: the step is a pure fp32 read-modify-write of the (B, D, N)
+// state plus a few bytes per token, so it is HBM bound (or L2 bound when the
+// state fits in the 126 MB L2).  Each thread owns four consecutive states of one
+// (b, d) row and moves them with one 16-byte load and one 16-byte store; the
+// N / 4 lanes of a row are adjacent, so a warp touches a contiguous 512-byte
+// span, and the readout is reduced with xor shuffles inside those lanes.
+#include "common.cuh"
+#include "internal.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kBlock = 256;
+
+template <typename TIO, int LPC, bool kFast, bool kVec>
+__global__ void __launch_bounds__(kBlock) decode_kernel(DecodeParams p) {
+    const TIO *__restrict__ gx = static_cast<const TIO *>(p.x);
+    const TIO *__restrict__ gdl = static_cast<const TIO *>(p.delta);
+    const TIO *__restrict__ gz = static_cast<const TIO *>(p.z);
+    const TIO *__restrict__ gB = static_cast<const TIO *>(p.Bm);
+    const TIO *__restrict__ gC = static_cast<const TIO *>(p.Cm);
+    TIO *__restrict__ gy = static_cast<TIO *>(p.y);
+
+    const int64_t D = p.dim;
+    const int N = static_cast<int>(p.dstate);
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    const int64_t row = gid / LPC;   // b * D + d
+    const int j = static_cast<int>(gid % LPC);
+    const bool valid = row < p.batch * D;
+    const int64_t b = valid ? row / D : 0;
+    const int64_t d = valid ? row % D : 0;
+
+    float acc = 0.f, xv = 0.f;
+    if (valid) {
+        xv = Io<TIO>::load(gx + row);
+        const float bias = p.bias ? p.bias[d] : 0.f;
+        const float dl = step_size<kFast>(Io<TIO>::load(gdl + row), bias, p.softplus);
+        const float dx = dl * xv;
+        const int n0 = j * 4;
+        float *st = p.state + row * N + n0;
+        float h[4];
+        if (kVec) {
+            const float4 s4 = *reinterpret_cast<const float4 *>(st);
+            h[0] = s4.x; h[1] = s4.y; h[2] = s4.z; h[3] = s4.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) h[k] = (n0 + k < N) ? st[k] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int n = n0 + k;
+            if (kVec || n < N) {
+                const float a = decay<kFast>(dl, scale_A<kFast>(p.A[d * N + n]));
+                h[k] = fmaf(a, h[k], dx * Io<TIO>::load(gB + b * N + n));
+                acc = fmaf(Io<TIO>::load(gC + b * N + n), h[k], acc);
+            }
+        }
+        if (kVec) {
+            *reinterpret_cast<float4 *>(st) = make_float4(h[0], h[1], h[2], h[3]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (n0 + k < N) st[k] = h[k];
+        }
+    }
+#pragma unroll
+    for (int off = LPC / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (valid && j == 0) {
+        float out = acc + (p.Dv ? p.Dv[d] * xv : 0.f);
+        if (gz) out *= silu<kFast>(Io<TIO>::load(gz + row));
+        gy[row] = Io<TIO>::from_f(out);
+    }
+}
+
+template <typename TIO, int LPC>
+cudaError_t launch_lpc(const DecodeParams &p, cudaStream_t stream) {
+    constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
+    const bool vec = (p.dstate == 4 * LPC) &&
+                     (reinterpret_cast<uintptr_t>(p.state) % 16 == 0);
+    const int64_t threads = p.batch * p.dim * LPC;
+    const unsigned grid = static_cast<unsigned>((threads + kBlock - 1) / kBlock);
+    if (vec)
+        decode_kernel<TIO, LPC, kFast, true><<<grid, kBlock, 0, stream>>>(p);
+    else
+        decode_kernel<TIO, LPC, kFast, false><<<grid, kBlock, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename TIO> cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream) {
+    const int64_t N = p.dstate;
+    if (N <= 4) return launch_lpc<TIO, 1>(p, stream);
+    if (N <= 8) return launch_lpc<TIO, 2>(p, stream);
+    if (N <= 16) return launch_lpc<TIO, 4>(p, stream);
+    if (N <= 32) return launch_lpc<TIO, 8>(p, stream);
+    return launch_lpc<TIO, 16>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream) {
+    return p.io_bf16 ? launch_typed<__nv_bfloat16>(p, stream) : launch_typed<float>(p, stream);
+}
+
+}  // namespace ssm

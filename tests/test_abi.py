@@ -1,0 +1,160 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, and rejects bad arguments on the host before touching CUDA.
+
+The pointer values used here are never dereferenced: every call below returns
+from the host-side checks (or the empty-problem shortcut) before any launch.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import selective_state_space_132_b300 as ssm
+from selective_state_space_132_b300 import binding as bd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm.h")
+
+OK, INVALID, UNSUPPORTED, ALIGN, WORKSPACE = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ssm.build_library()
+    return ssm.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SSM_API\s+[\w\s\*]+?\b(ssm_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    fns = header_functions()
+    for name in ("ssm_scan_fwd", "ssm_ssd_chunk_fwd", "ssm_step_decode",
+                 "ssm_scan_workspace_size", "ssm_ssd_workspace_size", "ssm_status_string",
+                 "ssm_version", "ssm_read_device_status"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", ssm.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)$", out, flags=re.M))
+    for name in header_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # nothing but the C ABI is exported
+    assert all(n.startswith("ssm_") or n.startswith("_") for n in exported), exported
+
+
+def test_version_and_status_strings(lib):
+    assert ssm.version() >= 10000
+    for code in range(7):
+        assert lib.ssm_status_string(code)
+    assert lib.ssm_status_string(99) == b"unknown status"
+
+
+def _scan(**kw):
+    base = dict(batch=2, seqlen=64, dim=32, dstate=16, time_chunk=0, io_dtype=1,
+                delta_softplus=1, x=0x10000, delta=0x20000, B=0x30000, C=0x40000, z=None,
+                A=0x50000, D=None, delta_bias=None, h0=None, y=0x60000, h_final=None,
+                workspace=None, workspace_bytes=0)
+    base.update(kw)
+    return bd.ScanArgs(**base)
+
+
+def _scan_rc(lib, **kw):
+    a = _scan(**kw)
+    return lib.ssm_scan_fwd(ctypes.byref(a), None)
+
+
+def test_scan_rejects_bad_arguments(lib):
+    assert lib.ssm_scan_fwd(None, None) == INVALID
+    assert _scan_rc(lib, dstate=0) == INVALID
+    assert _scan_rc(lib, batch=-1) == INVALID
+    assert _scan_rc(lib, io_dtype=7) == INVALID
+    assert _scan_rc(lib, delta_softplus=2) == INVALID
+    assert _scan_rc(lib, time_chunk=33) == INVALID
+    assert _scan_rc(lib, dstate=65) == UNSUPPORTED
+    assert _scan_rc(lib, batch=70000) == UNSUPPORTED
+    assert _scan_rc(lib, x=None) == INVALID
+    assert _scan_rc(lib, A=None) == INVALID
+    assert _scan_rc(lib, x=0x10001) == ALIGN            # bf16 needs 2-byte alignment
+    assert _scan_rc(lib, A=0x50002) == ALIGN            # fp32 needs 4-byte alignment
+    assert _scan_rc(lib, io_dtype=0, x=0x10002) == ALIGN
+    assert _scan_rc(lib, y=0x10000) == INVALID          # y aliases x
+    assert _scan_rc(lib, y=0x30010) == INVALID          # y overlaps B
+    # a forced time split needs a workspace
+    assert _scan_rc(lib, time_chunk=32) == WORKSPACE
+    need = ctypes.c_size_t(0)
+    a = _scan(time_chunk=32)
+    assert lib.ssm_scan_workspace_size(ctypes.byref(a), ctypes.byref(need)) == OK
+    assert need.value > 0
+    assert _scan_rc(lib, time_chunk=32, workspace=0x70000, workspace_bytes=need.value - 1) \
+        == WORKSPACE
+    assert _scan_rc(lib, time_chunk=32, workspace=0x70010, workspace_bytes=need.value) == ALIGN
+
+
+def test_scan_workspace_is_zero_without_time_split(lib):
+    assert ssm.scan_workspace_size(8, 2048, 1536, 16) == 0
+    assert ssm.scan_workspace_size(1, 131072, 2048, 16) > 0
+
+
+def test_empty_problems_return_without_launch(lib):
+    assert _scan_rc(lib, batch=0) == OK
+    assert _scan_rc(lib, dim=0, A=None) == OK
+
+
+def _ssd(**kw):
+    base = dict(batch=1, seqlen=64, nheads=4, headdim=64, ngroups=1, dstate=64, chunk_size=0,
+                io_dtype=1, delta_softplus=1, x=0x100000, delta=0x200000, B=0x300000,
+                C=0x400000, z=None, A=0x500000, D=None, delta_bias=None, h0=None,
+                y=0x600000, h_final=None, workspace=None, workspace_bytes=0)
+    base.update(kw)
+    return bd.SSDArgs(**base)
+
+
+def test_ssd_rejects_bad_arguments(lib):
+    def rc(**kw):
+        a = _ssd(**kw)
+        return lib.ssm_ssd_chunk_fwd(ctypes.byref(a), None)
+    assert rc(ngroups=3) == INVALID
+    assert rc(nheads=0) == INVALID
+    assert rc(dstate=257) == UNSUPPORTED
+    assert rc(A=None) == INVALID
+    assert rc(B=0x300001) == ALIGN
+    assert rc(y=0x100000) == INVALID
+    assert rc() == WORKSPACE
+    need = ctypes.c_size_t(0)
+    a = _ssd()
+    assert lib.ssm_ssd_workspace_size(ctypes.byref(a), ctypes.byref(need)) == OK
+    assert need.value >= 256
+    assert rc(workspace=0x700080, workspace_bytes=need.value) == ALIGN
+    assert rc(batch=0, workspace=0x700000, workspace_bytes=need.value) == OK
+
+
+def test_decode_rejects_bad_arguments(lib):
+    def rc(**kw):
+        base = dict(batch=4, dim=32, dstate=16, io_dtype=1, delta_softplus=1, state=0x100000,
+                    x=0x200000, delta=0x300000, B=0x400000, C=0x500000, z=None, A=0x600000,
+                    D=None, delta_bias=None, y=0x700000)
+        base.update(kw)
+        a = bd.DecodeArgs(**base)
+        return lib.ssm_step_decode(ctypes.byref(a), None)
+    assert rc(state=None) == INVALID
+    assert rc(dstate=0) == INVALID
+    assert rc(dstate=65) == UNSUPPORTED
+    assert rc(state=0x100002) == ALIGN
+    assert rc(y=0x200000) == INVALID
+    assert rc(y=0x100000) == INVALID                    # y inside the state
+    assert rc(batch=0) == OK
+
+
+def test_ops_fail_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(bd, "_lib", None)
+    monkeypatch.setattr(bd, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        bd.load_library()

@@ -1,0 +1,73 @@
+"""GPU parity of ssm_ssd_chunk_fwd (Mamba-2 SSD form) against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from selective_state_space_132_b300 import workloads as W
+
+from _parity import assert_close, run_scan, run_ssd
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(p, chunk=None):
+    y, hf = run_ssd(p, chunk)
+    yr, hr = oracle.ssd(**p.oracle_args())
+    assert np.all(np.isfinite(y))
+    assert_close(y, yr, p.io, "y")
+    assert_close(hf, hr, p.io, "h_final")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("P,N,G,H", [(64, 128, 1, 4), (64, 64, 2, 4), (16, 16, 1, 3),
+                                     (32, 128, 4, 8), (8, 5, 1, 2)])
+def test_shapes(io, P, N, G, H):
+    p = W.ssd_problem(2, 300, H, P, G, N, chunk=64, io=io, seed=60 + P + N, h0=True)
+    _check(p)
+
+
+@pytest.mark.parametrize("chunk", [32, 64, 128, 256])
+def test_chunk_sizes(chunk):
+    p = W.ssd_problem(1, 520, 4, 64, 1, 128, chunk=chunk, io="bf16", seed=70, gate=True)
+    _check(p, chunk)
+
+
+def test_gate_and_no_skip():
+    p = W.ssd_problem(2, 257, 4, 64, 1, 64, chunk=256, io="bf16", seed=71, gate=True,
+                      use_D=False, h0=True)
+    _check(p)
+
+
+def test_ssd_equals_scan_with_head_broadcast():
+    """An SSD head is an S6 scan over its P channels with a shared decay: run both on
+    the GPU and compare."""
+    p = W.ssd_problem(1, 200, 2, 16, 1, 16, chunk=64, io="f32", seed=72)
+    y, _ = run_ssd(p)
+    for h in range(p.heads):
+        s = W.scan_problem(1, 200, 16, 16, io="f32", seed=0, gate=False)
+        s.x = np.ascontiguousarray(p.x[:, :, h, :])
+        s.delta = np.ascontiguousarray(np.repeat(p.delta[:, :, h:h + 1], 16, axis=2))
+        s.A = np.full((16, 16), p.A[h], np.float32)
+        s.B, s.C = np.ascontiguousarray(p.B[:, :, 0]), np.ascontiguousarray(p.C[:, :, 0])
+        s.D = np.full(16, p.D[h], np.float32)
+        s.bias = np.full(16, p.bias[h], np.float32)
+        ys, _ = run_scan(s)
+        assert oracle.rel_l2(y[:, :, h, :], ys) < 2e-6
+
+
+@pytest.mark.slow
+def test_mamba2_full_size_sampled_heads():
+    """Reference workload: batch 4, L 8192, 80 heads x 64, N 128, one group, chunk 256,
+    bf16; the GPU runs it in full, the oracle checks 6 sampled (batch, head) pairs."""
+    p = W.config_problem(3)
+    y, hf = run_ssd(p)
+    pairs = [(0, 0), (0, 79), (1, 13), (2, 40), (3, 5), (3, 66)]
+    for b, h in pairs:
+        args = p.oracle_args()
+        args["x"] = p.x[b:b + 1, :, h:h + 1]
+        args["delta"] = p.delta[b:b + 1, :, h:h + 1]
+        args["Bm"], args["Cm"] = p.B[b:b + 1], p.C[b:b + 1]
+        args["A"], args["Dv"], args["bias"] = p.A[h:h + 1], p.D[h:h + 1], p.bias[h:h + 1]
+        yr, hr = oracle.ssd(**args)
+        assert_close(y[b:b + 1, :, h:h + 1], yr, "bf16", f"y[b={b},h={h}]")
+        assert_close(hf[b:b + 1, h:h + 1], hr, "bf16", f"h_final[b={b},h={h}]")
