@@ -1,0 +1,559 @@
+"""Benchmark of the selective-scan hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extras] [--no-cpu]
+
+One step = one forward pass of the S6 scan (softplus step, exp decay, state
+recurrence, C readout, D skip, SiLU gate) over one batch of the 130M-layer
+workload (batch 8, d_inner 1536, L 2048, N 16, bf16 I/O, fp32 state), inputs
+already resident in HBM, L2 flushed (a 256 MB write) before every step.  The
+metric is state updates per second (B*L*D*N / time).  Rank 0 prints one JSON
+line.  Under torchrun (N > 1) every rank runs its own independent batch (the
+chains of the scan are independent: no data-path collective), so scaling is
+weak and `value` is the updates of all ranks over the slowest rank's time.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from selective_state_space_132_b300 import workloads as W  # noqa: E402
+
+HBM_FALLBACK_GBS = 6400.0
+BF16_FALLBACK_TFLOPS = 1800.0
+L2_FLUSH_BYTES = 256 << 20
+
+# ncu DRAM traffic (bytes) per launch of the dominant kernel, keyed by the sha256
+# prefix of the kernel's sources at the time of the capture; an entry whose key no
+# longer matches the sources is ignored (traffic reported as null).
+PROFILED_TRAFFIC = {}
+
+WORKLOADS = {
+    "scan_bf16_B8_D1536_L2048_N16": 1,
+    "scan_bf16_B1_D2048_L131072_N16": 2,
+    "ssd_bf16_B4_L8192_H80_P64_N128_G1_Q256": 3,
+    "decode_bf16_B256_D5120_N16_x1000": 4,
+}
+SCAN_SOURCES = ["scan_fwd.cu", "common.cuh"]
+
+
+# ------------------------------------------------------------------ small helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(
+            d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, 1400.0, "fallback"
+
+
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "selective_state_space_132_b300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def scan_bytes(nb, L, D, N, e, gate=True, h0=False):
+    """Algorithmic bytes of one scan: x, delta (, z), y in the I/O dtype, B and C,
+    A, D and the bias in fp32, the final state (and h0) in fp32; no h_t."""
+    tok = nb * L * D * e
+    return (tok * (4 if gate else 3) + 2 * nb * L * N * e + D * N * 4 + 2 * D * 4
+            + nb * D * N * 4 * (2 if h0 else 1))
+
+
+def ssd_bytes(nb, L, H, P, G, N, e):
+    return (2 * nb * L * H * P * e + nb * L * H * e + 2 * nb * L * G * N * e + 3 * H * 4
+            + nb * H * P * N * 4)
+
+
+def decode_bytes_per_step(nb, D, N, e):
+    return 2 * nb * D * N * 4 + 4 * nb * D * e + 2 * nb * N * e + D * N * 4 + 2 * D * 4
+
+
+def ssd_flops(nb, L, H, P, G, N, Q):
+    """Dense tensor-core FLOPs of the chunked dual form: C B^T once per (b, chunk,
+    group), the causal half of (L o C B^T) X, the chunk states and C S^T."""
+    nc = (L + Q - 1) // Q
+    per_chunk_head = Q * Q * P + 2 * Q * P * N + 2 * Q * P * N
+    return nb * nc * (2 * Q * Q * N * G + H * per_chunk_head)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms in a thread."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1]
+        rows = inside or [s for (_, s) in self.samples]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [q.strip() for q in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, seconds_max: float, world: int) -> float:
+    """Whole-job throughput: every rank processed units_per_rank in at most seconds_max."""
+    return units_per_rank * world / seconds_max
+
+
+# ------------------------------------------------------------------ our arm
+def _to_dev(device):
+    import torch
+
+    def t(a, dtype=torch.float32):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(
+            device=device, dtype=dtype)
+    return t
+
+
+def time_scan(p, steps, warmup, flush, device, time_chunk=0):
+    """Per-step device time of ssm_scan_fwd on resident inputs, L2 flushed before each
+    step.  Returns (seconds per step, kernel launches per step, wall seconds, window)."""
+    import torch
+    import selective_state_space_132_b300 as ssm
+
+    io = torch.bfloat16 if p.io == "bf16" else torch.float32
+    t = _to_dev(device)
+    x, dl, z, Bm, Cm = t(p.x, io), t(p.delta, io), t(p.z, io), t(p.B, io), t(p.C, io)
+    A, Dv, bias = t(p.A), t(p.D), t(p.bias)
+    y = torch.empty_like(x)
+    hf = torch.empty((p.batch, p.dim, p.dstate), dtype=torch.float32, device=device)
+    nbytes = ssm.scan_workspace_size(p.batch, p.seqlen, p.dim, p.dstate, io, time_chunk)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    launches = ssm.scan_launches_per_call(p.batch, p.seqlen, p.dim, p.dstate, io, time_chunk)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ssm.scan_fwd(x, dl, A, Bm, Cm, D=Dv, z=z, delta_bias=bias, y=y, h_final=hf,
+                     workspace=ws, time_chunk=time_chunk, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0 = time.time()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.time() - t0
+    per = [a.elapsed_time(b) * 1e-3 for a, b in ev]
+    return per, launches, wall, (t0, t0 + wall)
+
+
+def e2e_scan(p, steps, device):
+    """Same metric through the public API with pinned host buffers: every step copies
+    the inputs host->device, runs the scan and reads y and the final state back."""
+    import torch
+    import selective_state_space_132_b300 as ssm
+
+    io = torch.bfloat16 if p.io == "bf16" else torch.float32
+
+    def pin(a, dtype=io):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dtype).pin_memory()
+    hx, hdl, hz, hB, hC = pin(p.x), pin(p.delta), pin(p.z), pin(p.B), pin(p.C)
+    A = torch.from_numpy(p.A).to(device)
+    Dv = torch.from_numpy(p.D).to(device)
+    bias = torch.from_numpy(p.bias).to(device)
+    hy = torch.empty(hx.shape, dtype=io).pin_memory()
+    hh = torch.empty((p.batch, p.dim, p.dstate), dtype=torch.float32).pin_memory()
+    h2d = sum(a.numel() * a.element_size() for a in (hx, hdl, hz, hB, hC))
+    d2h = hy.numel() * hy.element_size() + hh.numel() * hh.element_size()
+
+    def step():
+        x, dl, z = (a.to(device, non_blocking=True) for a in (hx, hdl, hz))
+        Bm, Cm = hB.to(device, non_blocking=True), hC.to(device, non_blocking=True)
+        y, hf = ssm.scan_fwd(x, dl, A, Bm, Cm, D=Dv, z=z, delta_bias=bias)
+        hy.copy_(y, non_blocking=True)
+        hh.copy_(hf, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) * 1e-3 / steps, h2d, d2h
+
+
+def time_ssd(p, iters, flush, device):
+    import torch
+    import selective_state_space_132_b300 as ssm
+    io = torch.bfloat16
+    t = _to_dev(device)
+    x, dl, Bm, Cm = t(p.x, io), t(p.delta, io), t(p.B, io), t(p.C, io)
+    A, Dv, bias = t(p.A), t(p.D), t(p.bias)
+    y = torch.empty_like(x)
+    hf = torch.empty((p.batch, p.heads, p.headdim, p.dstate), dtype=torch.float32,
+                     device=device)
+    ws = torch.empty(ssm.ssd_workspace_size(x, dl, A, Bm, Cm, p.chunk), dtype=torch.uint8,
+                     device=device)
+
+    def step():
+        ssm.ssd_chunk_fwd(x, dl, A, Bm, Cm, D=Dv, delta_bias=bias, chunk_size=p.chunk, y=y,
+                          h_final=hf, workspace=ws)
+    step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e-3)
+    return float(np.median(times))
+
+
+def time_decode(p, steps, flush, device, pool=8):
+    """Per-step time of ssm_step_decode with the state in place; tokens cycle through a
+    pool of `pool` pre-generated steps.  Returns (median with L2 flushed before each
+    step, mean over back-to-back steps)."""
+    import torch
+    import selective_state_space_132_b300 as ssm
+    io = torch.bfloat16
+    t = _to_dev(device)
+    state = t(p.state0)
+    A, Dv, bias = t(p.A), t(p.D), t(p.bias)
+    toks = []
+    for s in range(pool):
+        k = p.tokens(s)
+        toks.append({n: t(v, io) for n, v in k.items()})
+    y = torch.empty((p.batch, p.dim), dtype=io, device=device)
+
+    def step(i):
+        k = toks[i % pool]
+        ssm.step_decode(state, k["x"], k["delta"], A, k["B"], k["C"], D=Dv, z=k["z"],
+                        delta_bias=bias, y=y)
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    flushed = []
+    for i in range(min(steps, 50)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step(i)
+        b.record()
+        torch.cuda.synchronize()
+        flushed.append(a.elapsed_time(b) * 1e-3)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(steps):
+        step(i)
+    b.record()
+    torch.cuda.synchronize()
+    return float(np.median(flushed)), a.elapsed_time(b) * 1e-3 / steps
+
+
+def cpu_baseline_scan(p, target_s=10.0, max_s=30.0):
+    """The fp64 oracle as it stands, all host cores, on a bounded channel sample of
+    the workload; returns updates/s and what the sample was."""
+    import oracle
+    threads = oracle.default_threads()
+
+    def run(nch):
+        args = p.oracle_args()
+        sel = slice(0, nch)
+        for k in ("x", "delta", "z"):
+            args[k] = np.ascontiguousarray(getattr(p, k)[:, :, sel])
+        args["A"], args["Dv"], args["bias"] = p.A[sel], p.D[sel], p.bias[sel]
+        t0 = time.perf_counter()
+        oracle.scan(**args, threads=threads)
+        return time.perf_counter() - t0
+    nch = min(p.dim, 16)
+    dt = run(nch)
+    while dt < target_s / 4 and nch < p.dim:
+        nch = min(p.dim, nch * 4)
+        dt = run(nch)
+        if dt > max_s:
+            break
+    updates = p.batch * p.seqlen * nch * p.dstate
+    return {"value": updates / dt, "unit": "state-updates/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"batch {p.batch} x L {p.seqlen} x {nch} of {p.dim} channels x N "
+                      f"{p.dstate} ({updates:.3e} updates, {dt:.1f} s, fp64 C + OpenMP)"}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    hbm, tf_burst, tf_sus, peak_kind = measured_peaks()
+    p = W.config_problem(WORKLOADS[args.workload])
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    units = p.updates
+    e = 2 if p.io == "bf16" else 4
+    algo = scan_bytes(p.batch, p.seqlen, p.dim, p.dstate, e)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    per, launches, wall, window = time_scan(p, args.steps, args.warmup, flush, device)
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        time.sleep(0.1)
+        sampler.stop()
+    dev_s = float(np.sum(per))
+    sec_per_step = max_over_ranks(dev_s, world) / args.steps
+    value = aggregate(units, sec_per_step, world)
+    achieved = algo / float(np.mean(per)) / 1e9
+    src_hash = kernel_source_hash(SCAN_SOURCES)
+    out = {
+        "metric": "selective-scan state updates/s (B*L*D*N)",
+        "value": value, "unit": "state-updates/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec_per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; reference recipe)",
+        "config": {"workload": args.workload, "batch": p.batch, "seqlen": p.seqlen,
+                   "d_inner": p.dim, "d_state": p.dstate, "io": p.io, "state": "fp32",
+                   "gate": True, "l2": "flushed before every step (256 MB write)",
+                   "parallelism": f"replicas x{world} (independent batches per GPU)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": PROFILED_TRAFFIC.get(src_hash),
+                     "peak_kind": peak_kind, "algorithmic_bytes_per_launch": algo,
+                     "frac_of_nominal_8000": achieved / 8000.0, "source_hash": src_hash},
+        "gpu_launches": launches * args.steps,
+        "wall_ms_per_step_incl_flush": wall / args.steps * 1e3,
+    }
+    if rank == 0:
+        out["clocks"] = sampler.summary(*window) if sampler else None
+        e2e_s, h2d, d2h = e2e_scan(p, min(args.steps, 20), device)
+        out["e2e"] = {"value": units / e2e_s, "unit": "state-updates/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "ms_per_step": e2e_s * 1e3}
+        if world == 1 and not args.no_cpu:
+            out["cpu_baseline"] = cpu_baseline_scan(p)
+        if not args.no_extras and world == 1:
+            out["kernels"] = extras(device, flush, hbm, tf_sus)
+    return out
+
+
+def extras(device, flush, hbm, tf_sus):
+    """The other workloads, one measurement each (parity cases, not the bench line)."""
+    import torch
+    res = {}
+    p = W.config_problem(2)
+    per, launches, _, _ = time_scan(p, 5, 3, flush, device)
+    s = float(np.median(per))
+    b = scan_bytes(p.batch, p.seqlen, p.dim, p.dstate, 2)
+    res["scan_bf16_B1_D2048_L131072_N16"] = {
+        "ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
+        "hbm_frac": b / s / 1e9 / hbm, "launches": launches}
+    del p
+    p = W.config_problem(3)
+    s = time_ssd(p, 5, flush, device)
+    b = ssd_bytes(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, 2)
+    fl = ssd_flops(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, p.chunk)
+    res["ssd_bf16_B4_L8192_H80_P64_N128_G1_Q256"] = {
+        "ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
+        "hbm_frac": b / s / 1e9 / hbm, "tensor_tflops": fl / s / 1e12,
+        "tensor_frac_sustained": fl / s / 1e12 / tf_sus}
+    del p
+    torch.cuda.empty_cache()
+    p = W.config_problem(4)
+    s_flush, s_hot = time_decode(p, p.steps, flush, device)
+    b = decode_bytes_per_step(p.batch, p.dim, p.dstate, 2)
+    res["decode_bf16_B256_D5120_N16_x1000"] = {
+        "ms_per_step_l2_flushed": s_flush * 1e3, "ms_per_step_back_to_back": s_hot * 1e3,
+        "updates_per_s": p.updates_per_step / s_flush, "gbs_l2_flushed": b / s_flush / 1e9,
+        "hbm_frac_l2_flushed": b / s_flush / 1e9 / hbm,
+        "gbs_back_to_back": b / s_hot / 1e9,
+        "note": "back-to-back steps keep much of the 84 MB state in the 126 MB L2"}
+    return res
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, world):
+    """The fp64 oracle, as it stands, on the host cores; one step = one oracle run over
+    a bounded channel sample of the same workload."""
+    import oracle
+    p = W.config_problem(WORKLOADS[args.workload])
+    threads = oracle.default_threads()
+    budget_s = 120.0 / max(1, args.steps + args.warmup)
+
+    def make(nch):
+        a = p.oracle_args()
+        sel = slice(0, nch)
+        for k in ("x", "delta", "z"):
+            a[k] = np.ascontiguousarray(getattr(p, k)[:, :, sel], np.float64)
+        a["A"], a["Dv"], a["bias"] = p.A[sel], p.D[sel], p.bias[sel]
+        for k in ("Bm", "Cm"):
+            a[k] = np.ascontiguousarray(a[k], np.float64)
+        return a
+    nch = 8
+    a = make(nch)
+    t0 = time.perf_counter()
+    oracle.scan(**a, threads=threads)
+    rate = p.batch * p.seqlen * nch * p.dstate / (time.perf_counter() - t0)
+    nch = int(max(1, min(p.dim, rate * budget_s / (p.batch * p.seqlen * p.dstate))))
+    a = make(nch)
+    for _ in range(args.warmup):
+        oracle.scan(**a, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scan(**a, threads=threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    units = p.batch * p.seqlen * nch * p.dstate
+    value = units / dt
+    sample = (f"batch {p.batch} x L {p.seqlen} x {nch} of {p.dim} channels x N {p.dstate} "
+              f"per step ({units:.3e} updates)")
+    return {
+        "impl": "reference", "metric": "selective-scan state updates/s (B*L*D*N)",
+        "value": value, "unit": "state-updates/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; reference recipe)",
+        "config": {"workload": args.workload, "batch": p.batch, "seqlen": p.seqlen,
+                   "d_inner": p.dim, "d_state": p.dstate, "io": p.io},
+        "cpu_baseline": {"value": value, "unit": "state-updates/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "state-updates/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(k for k in WORKLOADS if k.startswith("scan")),
+                    default="scan_bf16_B8_D1536_L2048_N16")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        print(json.dumps(run_reference(args, world)))
+        return 0
+    world, rank, local = dist_setup()
+    out = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -99,6 +99,11 @@ typedef struct {
 } ssm_scan_args;
 
 SSM_API ssm_status ssm_scan_workspace_size(const ssm_scan_args *args, size_t *bytes);
+/* How ssm_scan_fwd will run these sizes (reads sizes and flags only): the time
+ * steps per chunk, the number of chunks along time, and the kernel launches per
+ * call (1 when the sequence is one chunk, 2 when a summary pass is needed). */
+SSM_API ssm_status ssm_scan_plan(const ssm_scan_args *args, int64_t *chunk_len,
+                                 int32_t *nchunks, int32_t *launches);
 SSM_API ssm_status ssm_scan_fwd(const ssm_scan_args *args, ssm_stream_t stream);
 
 /* ------------------------------------------------------------------ SSD (Mamba-2)

@@ -13,9 +13,10 @@ in the library's kernels; if the library is missing, the calls raise.
 from __future__ import annotations
 
 from .binding import (SSMError, build_library, library_path, load_library, scan_fwd,
-                      scan_workspace_size, ssd_chunk_fwd, ssd_workspace_size, step_decode,
-                      version)
+                      scan_launches_per_call, scan_plan, scan_workspace_size, ssd_chunk_fwd,
+                      ssd_workspace_size, step_decode, version)
 
 __all__ = ["SSMError", "build_library", "library_path", "load_library", "scan_fwd",
+           "scan_launches_per_call", "scan_plan",
            "scan_workspace_size", "ssd_chunk_fwd", "ssd_workspace_size", "step_decode",
            "version"]

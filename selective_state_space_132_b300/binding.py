@@ -16,7 +16,7 @@ _STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED",
            3: "SSM_ERR_ALIGNMENT", 4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA",
            6: "SSM_ERR_TIMEOUT"}
 
-EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_ssd_workspace_size",
+EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_ssd_workspace_size",
             "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_status_string", "ssm_version",
             "ssm_read_device_status"]
 
@@ -81,12 +81,14 @@ def load_library():
     lib.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanArgs),
                                             ctypes.POINTER(ctypes.c_size_t)]
     lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanArgs), _vp]
+    lib.ssm_scan_plan.argtypes = [ctypes.POINTER(ScanArgs), ctypes.POINTER(ctypes.c_int64),
+                                  ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     lib.ssm_ssd_workspace_size.argtypes = [ctypes.POINTER(SSDArgs),
                                            ctypes.POINTER(ctypes.c_size_t)]
     lib.ssm_ssd_chunk_fwd.argtypes = [ctypes.POINTER(SSDArgs), _vp]
     lib.ssm_step_decode.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
     lib.ssm_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
-    for fn in ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_ssd_workspace_size",
+    for fn in ("ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_ssd_workspace_size",
                "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_read_device_status"):
         getattr(lib, fn).restype = ctypes.c_int
     lib.ssm_status_string.argtypes = [ctypes.c_int]
@@ -177,11 +179,28 @@ def scan_workspace_size(batch: int, seqlen: int, dim: int, dstate: int,
                         io_dtype=torch.bfloat16, time_chunk: int = 0) -> int:
     a = ScanArgs(batch, seqlen, dim, dstate, int(time_chunk),
                  SSM_BF16 if io_dtype == torch.bfloat16 else SSM_F32, 1,
-                 1024, 1024, 1024, 1024, None, 1024, None, None, None, 4096, None, None, 0)
+                 None, None, None, None, None, None, None, None, None, None, None, None, 0)
     out = ctypes.c_size_t(0)
     _raise(load_library().ssm_scan_workspace_size(ctypes.byref(a), ctypes.byref(out)),
            "ssm_scan_workspace_size")
     return int(out.value)
+
+
+def scan_plan(batch: int, seqlen: int, dim: int, dstate: int, io_dtype=torch.bfloat16,
+              time_chunk: int = 0):
+    """(steps per time chunk, number of chunks, kernel launches per call)."""
+    a = ScanArgs(batch, seqlen, dim, dstate, int(time_chunk),
+                 SSM_BF16 if io_dtype == torch.bfloat16 else SSM_F32, 1,
+                 None, None, None, None, None, None, None, None, None, None, None, None, 0)
+    cl, k, n = ctypes.c_int64(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    _raise(load_library().ssm_scan_plan(ctypes.byref(a), ctypes.byref(cl), ctypes.byref(k),
+                                        ctypes.byref(n)), "ssm_scan_plan")
+    return int(cl.value), int(k.value), int(n.value)
+
+
+def scan_launches_per_call(batch, seqlen, dim, dstate, io_dtype=torch.bfloat16,
+                           time_chunk: int = 0) -> int:
+    return scan_plan(batch, seqlen, dim, dstate, io_dtype, time_chunk)[2]
 
 
 def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,

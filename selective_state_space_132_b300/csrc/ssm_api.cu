@@ -186,6 +186,20 @@ ssm_status ssm_scan_workspace_size(const ssm_scan_args *a, size_t *bytes) {
     return SSM_OK;
 }
 
+ssm_status ssm_scan_plan(const ssm_scan_args *a, int64_t *chunk_len, int32_t *nchunks,
+                         int32_t *launches) {
+    if (!chunk_len || !nchunks || !launches) return SSM_ERR_INVALID_ARG;
+    ssm_status s = check_scan(a, false);
+    if (s != SSM_OK) return s;
+    int64_t cl;
+    int k;
+    scan_ws(a, &cl, &k);
+    *chunk_len = cl;
+    *nchunks = k;
+    *launches = (a->batch == 0 || a->dim == 0) ? 0 : (k > 1 ? 2 : 1);
+    return SSM_OK;
+}
+
 ssm_status ssm_scan_fwd(const ssm_scan_args *a, ssm_stream_t stream) {
     ssm_status s = check_scan(a);
     if (s != SSM_OK) return s;

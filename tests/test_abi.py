@@ -98,6 +98,14 @@ def test_scan_rejects_bad_arguments(lib):
     assert _scan_rc(lib, time_chunk=32, workspace=0x70010, workspace_bytes=need.value) == ALIGN
 
 
+def test_scan_plan(lib):
+    assert ssm.scan_plan(8, 2048, 1536, 16) == (2048, 1, 1)          # one pass, no split
+    cl, k, n = ssm.scan_plan(1, 131072, 2048, 16)                   # long: split over time
+    assert k > 1 and n == 2 and cl % 32 == 0 and cl * k >= 131072
+    assert ssm.scan_plan(2, 300, 8, 16, time_chunk=64) == (64, 5, 2)
+    assert ssm.scan_plan(0, 300, 8, 16)[2] == 0
+
+
 def test_scan_workspace_is_zero_without_time_split(lib):
     assert ssm.scan_workspace_size(8, 2048, 1536, 16) == 0
     assert ssm.scan_workspace_size(1, 131072, 2048, 16) > 0

@@ -42,8 +42,10 @@ def test_state_sizes(io, N):
 def test_optional_inputs(gate, use_D, use_bias, softplus, h0):
     p = W.scan_problem(3, 150, 70, 16, io="bf16", seed=7, gate=gate, use_D=use_D,
                        use_bias=use_bias, softplus=softplus, h0=h0)
-    if not softplus:
-        p.delta = np.abs(p.delta)
+    if not softplus:  # keep the step positive: small |raw| plus a small positive bias
+        p.delta = W.round_bf16(np.abs(p.delta) * np.float32(0.1))
+        if p.bias is not None:
+            p.bias = np.abs(p.bias) * np.float32(0.01)
     _check(p)
 
 
