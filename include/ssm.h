@@ -106,6 +106,29 @@ SSM_API ssm_status ssm_scan_plan(const ssm_scan_args *args, int64_t *chunk_len,
                                  int32_t *nchunks, int32_t *launches);
 SSM_API ssm_status ssm_scan_fwd(const ssm_scan_args *args, ssm_stream_t stream);
 
+/* ------------------------------------------------------------------ scan without allocation
+ * No counterpart in the pages: a library convenience.  Same computation, arguments
+ * and results as ssm_scan_fwd, but the scratch that a time-split sequence needs
+ * comes from a fixed buffer inside the library instead of args->workspace (which
+ * is ignored), so the caller allocates nothing beyond its inputs and outputs.  It
+ * is meant for callers that cannot allocate device memory on the call path: a
+ * plugin inside another runtime that owns all device memory, a latency-critical
+ * loop that cannot afford cudaMalloc's implicit synchronisation, or a process
+ * limited to memory reserved at start-up.
+ *   - The buffer holds SSM_NOALLOC_SCRATCH_BYTES (4 MiB) on every GPU that loads
+ *     the library, until the process exits.  Problems whose scratch need, as
+ *     reported by ssm_scan_workspace_size, is larger are rejected with
+ *     SSM_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on a device looks up the buffer's device address for that
+ *     device (cudaGetSymbolAddress, with the device current); make that first
+ *     call before any stream capture.  No call allocates memory.
+ *   - Every call on a device shares the one buffer and leaves its contents behind;
+ *     the call clears what must start at zero itself.  Calls whose work overlaps
+ *     on the GPU (other streams, other host threads) race on the buffer: order
+ *     them on one stream or synchronise between them. */
+#define SSM_NOALLOC_SCRATCH_BYTES (4u << 20)
+SSM_API ssm_status ssm_scan_fwd_noalloc(const ssm_scan_args *args, ssm_stream_t stream);
+
 /* ------------------------------------------------------------------ SSD (Mamba-2)
  * Shapes (H = nheads, P = headdim, G = ngroups, N = dstate; head h reads group
  * h / (H / G)):

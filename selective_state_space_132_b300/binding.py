@@ -16,7 +16,7 @@ _STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED",
            3: "SSM_ERR_ALIGNMENT", 4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA",
            6: "SSM_ERR_TIMEOUT"}
 
-EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_ssd_workspace_size",
+EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc", "ssm_ssd_workspace_size",
             "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_status_string", "ssm_version",
             "ssm_read_device_status"]
 
@@ -81,6 +81,7 @@ def load_library():
     lib.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanArgs),
                                             ctypes.POINTER(ctypes.c_size_t)]
     lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanArgs), _vp]
+    lib.ssm_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ScanArgs), _vp]
     lib.ssm_scan_plan.argtypes = [ctypes.POINTER(ScanArgs), ctypes.POINTER(ctypes.c_int64),
                                   ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     lib.ssm_ssd_workspace_size.argtypes = [ctypes.POINTER(SSDArgs),
@@ -88,7 +89,7 @@ def load_library():
     lib.ssm_ssd_chunk_fwd.argtypes = [ctypes.POINTER(SSDArgs), _vp]
     lib.ssm_step_decode.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
     lib.ssm_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
-    for fn in ("ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_ssd_workspace_size",
+    for fn in ("ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc", "ssm_ssd_workspace_size",
                "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_read_device_status"):
         getattr(lib, fn).restype = ctypes.c_int
     lib.ssm_status_string.argtypes = [ctypes.c_int]
@@ -227,6 +228,24 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
     ws, nbytes = _workspace(int(need.value), x.device, workspace)
     args.workspace, args.workspace_bytes = _ptr(ws), nbytes
     _raise(lib.ssm_scan_fwd(ctypes.byref(args), _stream(stream)), "ssm_scan_fwd")
+    return y, h_final
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def scan_fwd_noalloc(x, delta, A, B, C, D=None, z=None, delta_bias=None,
+                     delta_softplus: bool = True, h0=None, y=None, h_final=None,
+                     time_chunk: int = 0, stream=None):
+    """ssm_scan_fwd_noalloc: the scan with the library's fixed scratch buffer instead
+    of a workspace, for callers that must not allocate device memory per call.
+    Outputs y and h_final must be passed in (nothing is allocated here either)."""
+    if y is None:
+        raise ValueError("scan_fwd_noalloc allocates nothing: pass y (and h_final if wanted)")
+    args = _scan_args(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final,
+                      time_chunk)
+    _raise(load_library().ssm_scan_fwd_noalloc(ctypes.byref(args), _stream(stream)),
+           "ssm_scan_fwd_noalloc")
     return y, h_final
 
 

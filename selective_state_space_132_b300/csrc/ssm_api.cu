@@ -159,6 +159,11 @@ ssm_status check_decode(const ssm_decode_args *a) {
 
 }  // namespace
 
+namespace ssm {
+// Full argument check of a scan call (sizes, flags, pointers), for other entry points.
+ssm_status check_scan_args(const ssm_scan_args *a) { return check_scan(a, true); }
+}  // namespace ssm
+
 extern "C" {
 
 const char *ssm_status_string(ssm_status s) {

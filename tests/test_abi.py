@@ -144,6 +144,24 @@ def test_ssd_rejects_bad_arguments(lib):
     assert rc(batch=0, workspace=0x700000, workspace_bytes=need.value) == OK
 
 
+def test_noalloc_scan_rejects_problems_beyond_its_scratch(lib):
+    """Sizes whose chunk summaries exceed the fixed 4 MiB buffer are refused on the
+    host, before any CUDA call (so this runs without a GPU)."""
+    from conftest import cuda_available
+    if cuda_available():
+        pytest.skip("uses fake device pointers; checked on CPU-only hosts")
+    # 64 chunks x 1024 channels x (16 + 1) floats > 4 MiB
+    far = dict(x=1 << 32, delta=2 << 32, B=3 << 32, C=4 << 32, A=5 << 32, y=6 << 32)
+    a = _scan(batch=1, seqlen=2048, dim=1024, time_chunk=32, **far)
+    need = ctypes.c_size_t(0)
+    assert lib.ssm_scan_workspace_size(ctypes.byref(a), ctypes.byref(need)) == OK
+    assert need.value > bd.NOALLOC_SCRATCH_BYTES
+    assert lib.ssm_scan_fwd_noalloc(ctypes.byref(a), None) == UNSUPPORTED
+    assert lib.ssm_scan_fwd_noalloc(None, None) == INVALID
+    assert lib.ssm_scan_fwd_noalloc(ctypes.byref(_scan(x=0x10001)), None) == ALIGN
+    assert lib.ssm_scan_fwd_noalloc(ctypes.byref(_scan(batch=0)), None) == OK
+
+
 def test_decode_rejects_bad_arguments(lib):
     def rc(**kw):
         base = dict(batch=4, dim=32, dstate=16, io_dtype=1, delta_softplus=1, state=0x100000,
