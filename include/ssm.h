@@ -83,8 +83,9 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
  * a positive value (a multiple of 32) forces it, which splits long sequences over
  * several blocks joined by a carry pass (exact up to rounding).
  * Workspace: ssm_scan_workspace_size() bytes (it reads only the sizes and flags of
- * `args`, not the pointers; 0 means none is needed), 256-byte aligned; contents
- * need no initialisation. */
+ * `args`, not the pointers), 256-byte aligned, always required: its first 256 bytes
+ * hold the device status word (cleared by the call itself), the rest the chunk
+ * summaries of a time-split sequence; contents need no initialisation. */
 typedef struct {
     int64_t batch, seqlen, dim, dstate;
     int64_t time_chunk;
@@ -135,9 +136,13 @@ SSM_API ssm_status ssm_scan_fwd_noalloc(const ssm_scan_args *args, ssm_stream_t 
  *   x, z, y : (B, L, H, P) io_dtype     delta : (B, L, H) io_dtype
  *   B, C    : (B, L, G, N) io_dtype     A, D, delta_bias : (H) fp32
  *   h0, h_final : (B, H, P, N) fp32
- * Nullable: D, delta_bias, z, h0, h_final.  H % G == 0.  chunk_size: the chunk
- * length Q of the dual form (0 = 256); the result does not depend on it beyond
- * rounding.  Workspace: ssm_ssd_workspace_size() bytes, 256-byte aligned. */
+ * Nullable: D, delta_bias, z, h0, h_final.  H % G == 0.  chunk_size (>= 0): the
+ * chunk length Q asked for the dual form.  The tensor-core kernel (bf16 I/O, P = 64,
+ * N = 128) always works in 128-step chunks: a longer chunk is the same sum with its
+ * below-diagonal 128 x 128 blocks factored through the state at the block boundary,
+ * so the result does not depend on chunk_size beyond rounding.  Other shapes run a
+ * sequential recurrence kernel.  Workspace: ssm_ssd_workspace_size() bytes,
+ * 256-byte aligned (its first 256 bytes hold the device status word). */
 typedef struct {
     int64_t batch, seqlen, nheads, headdim, ngroups, dstate;
     int64_t chunk_size;
@@ -153,6 +158,10 @@ typedef struct {
 
 SSM_API ssm_status ssm_ssd_workspace_size(const ssm_ssd_args *args, size_t *bytes);
 SSM_API ssm_status ssm_ssd_chunk_fwd(const ssm_ssd_args *args, ssm_stream_t stream);
+/* Which kernel ssm_ssd_chunk_fwd runs for these arguments (reads sizes, flags and
+ * pointer alignment): 1 = the chunked dual form on tcgen05 tensor cores (chunk 128),
+ * 0 = the sequential recurrence. */
+SSM_API ssm_status ssm_ssd_plan(const ssm_ssd_args *args, int32_t *tensor_core);
 
 /* ------------------------------------------------------------------ decode step
  * Shapes: state (B, D, N) fp32, read and written IN PLACE;

@@ -14,9 +14,10 @@ from __future__ import annotations
 
 from .binding import (SSMError, build_library, library_path, load_library, scan_fwd,
                       scan_launches_per_call, scan_plan, scan_workspace_size, ssd_chunk_fwd,
-                      ssd_workspace_size, step_decode, version)
+                      ssd_uses_tensor_cores, ssd_workspace_size, step_decode, version)
 
 __all__ = ["SSMError", "build_library", "library_path", "load_library", "scan_fwd",
            "scan_launches_per_call", "scan_plan",
-           "scan_workspace_size", "ssd_chunk_fwd", "ssd_workspace_size", "step_decode",
+           "scan_workspace_size", "ssd_chunk_fwd", "ssd_uses_tensor_cores", "ssd_workspace_size",
+           "step_decode",
            "version"]

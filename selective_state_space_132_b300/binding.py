@@ -16,8 +16,9 @@ _STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED",
            3: "SSM_ERR_ALIGNMENT", 4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA",
            6: "SSM_ERR_TIMEOUT"}
 
-EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc", "ssm_ssd_workspace_size",
-            "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_status_string", "ssm_version",
+EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
+            "ssm_ssd_workspace_size", "ssm_ssd_chunk_fwd", "ssm_ssd_plan", "ssm_step_decode",
+            "ssm_status_string", "ssm_version",
             "ssm_read_device_status"]
 
 _i64, _i32, _vp, _fp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p
@@ -87,10 +88,12 @@ def load_library():
     lib.ssm_ssd_workspace_size.argtypes = [ctypes.POINTER(SSDArgs),
                                            ctypes.POINTER(ctypes.c_size_t)]
     lib.ssm_ssd_chunk_fwd.argtypes = [ctypes.POINTER(SSDArgs), _vp]
+    lib.ssm_ssd_plan.argtypes = [ctypes.POINTER(SSDArgs), ctypes.POINTER(ctypes.c_int32)]
     lib.ssm_step_decode.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
     lib.ssm_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
-    for fn in ("ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc", "ssm_ssd_workspace_size",
-               "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_read_device_status"):
+    for fn in ("ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
+               "ssm_ssd_workspace_size", "ssm_ssd_chunk_fwd", "ssm_ssd_plan", "ssm_step_decode",
+               "ssm_read_device_status"):
         getattr(lib, fn).restype = ctypes.c_int
     lib.ssm_status_string.argtypes = [ctypes.c_int]
     lib.ssm_status_string.restype = ctypes.c_char_p
@@ -279,6 +282,16 @@ def ssd_workspace_size(x, delta, A, B, C, chunk_size: int = 256) -> int:
     _raise(load_library().ssm_ssd_workspace_size(ctypes.byref(args), ctypes.byref(out)),
            "ssm_ssd_workspace_size")
     return int(out.value)
+
+
+def ssd_uses_tensor_cores(x, delta, A, B, C, z=None, y=None, chunk_size: int = 0) -> bool:
+    """Whether ssd_chunk_fwd takes the tcgen05 chunked kernel for these tensors."""
+    if y is None:
+        y = torch.empty_like(x)
+    args = _ssd_args(x, delta, A, B, C, None, z, None, True, None, y, None, chunk_size)
+    out = ctypes.c_int32(0)
+    _raise(load_library().ssm_ssd_plan(ctypes.byref(args), ctypes.byref(out)), "ssm_ssd_plan")
+    return bool(out.value)
 
 
 def ssd_chunk_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,

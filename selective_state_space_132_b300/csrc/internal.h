@@ -20,12 +20,29 @@ struct ScanParams {
     int nchunks;        // K
     float *hloc;        // (B, K, D, N) local end states of chunks 0..K-2
     float *dsum;        // (B, K, D) sum of steps of chunks 0..K-2
-    bool vec_ok;        // 16-byte vector loads allowed
+    void *status;       // DeviceStatus at the start of the workspace (may be null)
+    int clear_status;   // the first block of this launch clears the status word
 };
 
-// Number of time chunks and chunk length the scan uses for these sizes.
+// Lanes per channel of the TMA scan at N = 16 (2: 8 states per lane, 16
+// channels per block; 4: 4 states per lane, 8 channels per block).
+#ifndef SSM_SCAN_LANES16
+#define SSM_SCAN_LANES16 4
+#endif
+constexpr int kScanLanes16 = SSM_SCAN_LANES16;
+
+// TMA-staged scan (scan_tma.cu): lanes per channel for N (0 = not supported),
+// whether a call can take it, and the launch.
+int scan_tma_lanes(int64_t dstate);
+bool scan_tma_sizes_ok(int io_bf16, int64_t seqlen, int64_t dim, int64_t dstate);
+bool scan_tma_pointers_ok(const void *const *ptrs, int nptrs);
+int device_sm_count();
+cudaError_t launch_scan_tma(const ScanParams &p, cudaStream_t stream);
+
+// Number of time chunks and chunk length the scan uses for these sizes; `tma`
+// selects the plan of the TMA-staged path (its blocks hold 32 / lanes channels).
 void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t time_chunk,
-               int64_t *chunk_len, int *nchunks);
+               bool tma, int64_t *chunk_len, int *nchunks);
 size_t scan_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, int nchunks);
 cudaError_t launch_scan(const ScanParams &p, cudaStream_t stream);
 
@@ -55,5 +72,8 @@ struct SSDParams {
 size_t ssd_workspace_bytes(const SSDParams &p);
 cudaError_t launch_ssd(const SSDParams &p, cudaStream_t stream);
 cudaError_t launch_ssd_recurrent(const SSDParams &p, cudaStream_t stream);
+// Chunked dual form on tcgen05 (ssd_tc.cu): bf16 I/O, headdim 64, dstate 128.
+bool ssd_tc_eligible(const SSDParams &p);
+cudaError_t launch_ssd_tc(const SSDParams &p, cudaStream_t stream);
 
 }  // namespace ssm

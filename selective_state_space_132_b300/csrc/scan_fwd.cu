@@ -339,16 +339,36 @@ int lanes_for(int64_t N) { return N <= 4 ? 1 : N <= 8 ? 2 : N <= 16 ? 4 : 8; }
 
 }  // namespace
 
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+        cudaGetLastError();
+        return 148;  // B300
+    }
+    return sms;
+}
+
 void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t time_chunk,
-               int64_t *chunk_len, int *nchunks) {
+               bool tma, int64_t *chunk_len, int *nchunks) {
     int64_t cl;
     if (time_chunk > 0) {
         cl = (time_chunk + kTT - 1) / kTT * kTT;
     } else {
-        // enough warps to cover 148 SMs about eight deep; each extra chunk costs a
-        // summary pass (~3/4 of a scan of that chunk), so split only when short of it
-        const int64_t warps = batch * ((dim + kDT - 1) / kDT) * lanes_for(dstate);
-        const int64_t target = 148 * 8;
+        // Enough warps to fill every SM about eight (general kernel) or ten (TMA
+        // kernel, one warp per block) deep.  Each extra chunk costs a summary pass
+        // over that chunk (most of a scan of it), so split only when short of it and
+        // keep chunks at least 1024 steps long.
+        int64_t warps, target;
+        if (tma) {
+            const int64_t cpw = 32 / scan_tma_lanes(dstate);
+            warps = batch * ((dim + cpw - 1) / cpw);
+            target = static_cast<int64_t>(device_sm_count()) * 10;
+        } else {
+            warps = batch * ((dim + kDT - 1) / kDT) * lanes_for(dstate);
+            target = static_cast<int64_t>(device_sm_count()) * 8;
+        }
         int64_t k = warps > 0 ? (target + warps - 1) / warps : 1;
         const int64_t kmax = std::max<int64_t>(1, seqlen / 1024);
         k = std::max<int64_t>(1, std::min(k, kmax));
@@ -361,7 +381,7 @@ void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64
 }
 
 size_t scan_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, int nchunks) {
-    size_t bytes = kStatusBytes;
+    size_t bytes = kStatusBytes;  // device status word
     if (nchunks > 1) {
         const size_t rows = static_cast<size_t>(batch) * nchunks * dim;
         const size_t hl = rows * dstate * sizeof(float);
@@ -372,6 +392,9 @@ size_t scan_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, int nchu
 }
 
 cudaError_t launch_scan(const ScanParams &p, cudaStream_t stream) {
+    const void *ptrs[] = {p.x, p.delta, p.Bm, p.Cm, p.z, p.y};
+    if (scan_tma_sizes_ok(p.io_bf16, p.seqlen, p.dim, p.dstate) && scan_tma_pointers_ok(ptrs, 6))
+        return launch_scan_tma(p, stream);
     return p.io_bf16 ? launch_typed<__nv_bfloat16>(p, stream) : launch_typed<float>(p, stream);
 }
 

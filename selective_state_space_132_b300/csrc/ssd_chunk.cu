@@ -8,8 +8,8 @@
 //
 // This file holds the sequential-recurrence kernel: one lane group per (b, h, p)
 // row of the state, N / NS lanes per row, walking time in order.  It is the
-// general-shape path (any P, N <= 256, any G); the chunked tensor-core form
-// (ssd_tc.cu) is used where its shape rules hold.
+// general-shape path (any P, N <= 256, any G, fp32 or bf16); the chunked
+// tensor-core form (ssd_tc.cu) runs where its shape rules hold.
 #include "common.cuh"
 #include "internal.h"
 
@@ -114,6 +114,7 @@ cudaError_t launch_ssd_recurrent(const SSDParams &p, cudaStream_t stream) {
 size_t ssd_workspace_bytes(const SSDParams &) { return kStatusBytes; }
 
 cudaError_t launch_ssd(const SSDParams &p, cudaStream_t stream) {
+    if (ssd_tc_eligible(p)) return launch_ssd_tc(p, stream);
     return launch_ssd_recurrent(p, stream);
 }
 

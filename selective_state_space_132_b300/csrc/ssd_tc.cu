@@ -1,0 +1,467 @@
+// Multi-head selective SSM with a scalar decay per head (Mamba-2), computed in its
+// chunked dual form on the tcgen05 tensor cores.
+//
+// What it computes ("Mamba-2: 상태 공간 기반 시퀀스 모델", sections "1-세미분리 행렬",
+// "SSM-Attention 동치성", "멀티-헤드 구조" and "SSD 타일링 알고리즘"), per batch b and
+// head h (group g = h / (H / G)), with dl_t = softplus(delta_t,h + bias_h):
+//   S_t = exp(dl_t A_h) S_{t-1} + dl_t x_t B_t^T            (P x N state)
+//   y_t = S_t C_t + D_h x_t            (optionally times silu(z_t))
+// Inside a chunk of Q = 128 steps starting from state S_in, with the running
+// log-decay Lam_t = sum_{r <= t} dl_r A_h (inclusive, from the chunk start):
+//   G      = C B^T                                         (Q x Q, shared by heads)
+//   M[t,s] = G[t,s] exp(Lam_t - Lam_s) dl_s   for s <= t, else 0
+//   Y      = M X + diag(exp(Lam_t)) C S_in^T + D X         (the 1-semiseparable
+//                                                           matrix applied blockwise)
+//   S_out  = exp(Lam_end) S_in + (B^T Xw)^T,  Xw[s,:] = exp(Lam_end - Lam_s) dl_s x_s
+// which is the pages' intra-chunk (L o C B^T) X plus inter-chunk state passing
+// with the decay weights written out.  Chunk length: the pages' tiling uses 256
+// steps (tuned for A100); on B300 the M = 128 tcgen05 tile and the 512-column TMEM
+// make 128 the natural chunk.  A longer requested chunk is evaluated as 128-step
+// tiles whose below-diagonal block goes through the state at the tile boundary,
+// which is the same sum factored through rank N.
+//
+// B300 mapping (one thread block per (b, h) chain, 128 threads = one TMEM lane each):
+//   * TMA (128-byte swizzle) brings C, B (Q x N), X (Q x P) and z of a chunk into
+//     shared memory in the canonical UMMA layouts.
+//   * Four bf16 MMAs per chunk with fp32 accumulators in TMEM:
+//       G  = C B^T        (M=128, N=128, K=N)   A=C  K-major, B=B  K-major
+//       Yo = C S_in^T     (M=128, N=P,   K=N)   A=C  K-major, B=S  MN-major
+//       Sc = B^T Xw       (M=N=128, N=P, K=Q)   A=B  MN-major, B=Xw MN-major
+//       Yd = M X          (M=128, N=P,   K=Q)   A=M  K-major, B=X  MN-major
+//   * CUDA cores build Xw and M (masked exponentials, bf16) straight into shared
+//     memory in the swizzled layout, update the fp32 state held in registers
+//     (thread n owns row n of S^T) and finish y = Yd + exp(Lam_t) Yo + D x, which
+//     goes back to HBM through a TMA store.
+// Shape rules of this kernel: bf16 I/O, P = 64, N = 128; other shapes run the
+// sequential kernel (ssd_chunk.cu).
+#include <cudaTypedefs.h>
+
+#include "../../include/ssm.h"
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ssm {
+namespace {
+
+using ptx::f2;
+
+constexpr int kQ = 128;   // chunk length (MMA M)
+constexpr int kP = 64;    // head dim
+constexpr int kN = 128;   // state size
+constexpr int kThreads = 128;
+constexpr int kTmemCols = 512;
+// TMEM column offsets of the accumulators
+constexpr uint32_t kColG = 0, kColYd = 128, kColYo = 192, kColSc = 256;
+
+// Shared-memory layout (bytes); every operand tile starts on a 1024-byte boundary.
+constexpr int kTile = kQ * 128;                 // 128 rows x 128 bytes = 16 KB
+constexpr int o_C = 0;                          // 2 k-blocks of 64 states
+constexpr int o_B = o_C + 2 * kTile;
+constexpr int o_X = o_B + 2 * kTile;            // also the y staging tile
+constexpr int o_Z = o_X + kTile;
+constexpr int o_M = o_Z + kTile;                // 2 k-blocks of 64 steps
+constexpr int o_Xw = o_M + 2 * kTile;
+constexpr int o_S = o_Xw + kTile;               // S_in^T: 128 state rows x 64 p
+constexpr int o_dl = o_S + kTile;               // float[128]
+constexpr int o_lam = o_dl + kQ * 4;            // float[128]
+constexpr int o_red = o_lam + kQ * 4;           // float[4] warp totals
+constexpr int o_bar = o_red + 64;               // 2 mbarriers
+constexpr int o_tmem = o_bar + 16;
+constexpr int kSmemBytes = o_tmem + 16 + 1024;  // + slack to align the base to 1024
+
+struct Maps {
+    CUtensorMap C, B, X, Z, Y;
+};
+
+// 16-byte chunk `chunk` of row `row` in a tile of 128-byte rows stored with the
+// 128-byte swizzle (chunk index XOR row % 8), the layout TMA writes and UMMA reads.
+__device__ __forceinline__ uint4 ld_chunk(const unsigned char *tile, uint32_t row, uint32_t chunk) {
+    return *reinterpret_cast<const uint4 *>(tile + row * 128u + ((chunk ^ (row & 7u)) << 4));
+}
+__device__ __forceinline__ void st_chunk(unsigned char *tile, uint32_t row, uint32_t chunk, uint4 v) {
+    *reinterpret_cast<uint4 *>(tile + row * 128u + ((chunk ^ (row & 7u)) << 4)) = v;
+}
+
+template <bool kGate>
+__global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_constant__ Maps maps,
+                                                             SSDParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *sC = smem + o_C, *sB = smem + o_B, *sX = smem + o_X, *sZ = smem + o_Z;
+    unsigned char *sM = smem + o_M, *sXw = smem + o_Xw, *sS = smem + o_S;
+    float *s_dl = reinterpret_cast<float *>(smem + o_dl);
+    float *s_lam = reinterpret_cast<float *>(smem + o_lam);
+    float *s_red = reinterpret_cast<float *>(smem + o_red);
+    uint64_t *bar_load = reinterpret_cast<uint64_t *>(smem + o_bar);
+    uint64_t *bar_mma = bar_load + 1;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + o_tmem);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int64_t H = p.nheads, L = p.seqlen;
+    const int g = static_cast<int>(h / (H / p.ngroups));
+    const __nv_bfloat16 *gdt = static_cast<const __nv_bfloat16 *>(p.delta);
+    DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
+
+    const float a_l2 = p.A[h] * kLog2e;  // decay exponent per unit step, base 2
+    const float bias = p.bias ? p.bias[h] : 0.f;
+    const float Dh = p.Dv ? p.Dv[h] : 0.f;
+
+    if (tid == 0) {
+        ptx::mbar_init(bar_load, 1);
+        ptx::mbar_init(bar_mma, 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(s_tmem, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    // fp32 state, row n = tid of S^T: S[p][n] for p = 0..63
+    float S[kP];
+    {
+        const float *h0 = p.h0 ? p.h0 + (static_cast<int64_t>(b) * H + h) * kP * kN : nullptr;
+#pragma unroll
+        for (int pp = 0; pp < kP; ++pp) S[pp] = h0 ? h0[pp * kN + tid] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            uint4 v;
+            v.x = ptx::f2_to_bf2(S[8 * q + 0], S[8 * q + 1]);
+            v.y = ptx::f2_to_bf2(S[8 * q + 2], S[8 * q + 3]);
+            v.z = ptx::f2_to_bf2(S[8 * q + 4], S[8 * q + 5]);
+            v.w = ptx::f2_to_bf2(S[8 * q + 6], S[8 * q + 7]);
+            st_chunk(sS, tid, q, v);
+        }
+    }
+    ptx::fence_proxy_async_smem();  // the first Yo MMA reads sS
+
+    const uint32_t id_G = ptx::idesc_bf16(128, 128, 0, 0);
+    const uint32_t id_Yo = ptx::idesc_bf16(128, kP, 0, 1);
+    const uint32_t id_Sc = ptx::idesc_bf16(128, kP, 1, 1);
+    const uint32_t id_Yd = ptx::idesc_bf16(128, kP, 0, 1);
+    const uint32_t aC = ptx::smem_u32(sC), aB = ptx::smem_u32(sB), aX = ptx::smem_u32(sX);
+    const uint32_t aM = ptx::smem_u32(sM), aXw = ptx::smem_u32(sXw), aS = ptx::smem_u32(sS);
+    constexpr uint32_t kLoadBytes = 4 * kTile + (kGate ? 2 : 1) * kTile;
+
+    uint32_t ph_load = 0, ph_mma = 0;
+    bool ok = true;
+    int pending = 0;  // 1: a TMA load, 2: an MMA commit that did not arrive in time
+    // Every thread waits; the block agrees on the outcome so that it never splits.
+    auto wait_all = [&](uint64_t *bar, uint32_t ph) -> bool {
+        const int mine = ptx::mbar_wait(bar, ph) ? 1 : 0;
+        return __syncthreads_and(mine) != 0;
+    };
+    const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
+
+    for (int c = 0; c < nchunks && ok; ++c) {
+        const int t0 = c * kQ;
+        // ---- (a) loads of this chunk (the previous chunk released every tile)
+        if (tid == 0) {
+            ptx::bulk_wait_read<0>();  // y store of the previous chunk has left sX
+            ptx::mbar_arrive_expect_tx(bar_load, kLoadBytes);
+            for (int kb = 0; kb < 2; ++kb) {
+                ptx::tma_load_3d(sC + kb * kTile, &maps.C, bar_load, g * kN + 64 * kb, t0, b);
+                ptx::tma_load_3d(sB + kb * kTile, &maps.B, bar_load, g * kN + 64 * kb, t0, b);
+            }
+            ptx::tma_load_3d(sX, &maps.X, bar_load, h * kP, t0, b);
+            if (kGate) ptx::tma_load_3d(sZ, &maps.Z, bar_load, h * kP, t0, b);
+        }
+        // ---- (b) step sizes and the running log2-decay
+        const int64_t t = t0 + tid;
+        float dl = 0.f;
+        if (t < L) {
+            const float raw = __bfloat162float(gdt[(static_cast<int64_t>(b) * L + t) * H + h]);
+            dl = step_size<true>(raw, bias, p.softplus);
+        }
+        float lam = dl * a_l2;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float v = __shfl_up_sync(0xffffffffu, lam, off);
+            if (lane >= off) lam += v;
+        }
+        if (lane == 31) s_red[warp] = lam;
+        __syncthreads();
+        for (int w = 0; w < warp; ++w) lam += s_red[w];
+        s_dl[tid] = dl;
+        s_lam[tid] = lam;
+        __syncthreads();
+        const float lam_end = s_lam[kQ - 1];
+
+        if (!wait_all(bar_load, ph_load)) {
+            ok = false;
+            pending = 1;
+            break;
+        }
+        ph_load ^= 1;
+
+        // ---- (d) G = C B^T and Yo = C S_in^T
+        if (tid == 0) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kN / 16; ++k) {
+                const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
+                const uint64_t da = ptx::sdesc_sw128(aC + off, 16, 1024);
+                const uint64_t db = ptx::sdesc_sw128(aB + off, 16, 1024);
+                ptx::mma_bf16(tmem + kColG, da, db, id_G, k > 0);
+            }
+#pragma unroll
+            for (int k = 0; k < kN / 16; ++k) {
+                const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
+                const uint64_t da = ptx::sdesc_sw128(aC + off, 16, 1024);
+                const uint64_t db = ptx::sdesc_sw128(aS + k * 2048, 1024, 1024);
+                ptx::mma_bf16(tmem + kColYo, da, db, id_Yo, k > 0);
+            }
+        }
+        // ---- (e) Xw[s, :] = exp(Lam_end - Lam_s) dl_s x_s  (row s = tid)
+        {
+            const float w = ex2_approx(lam_end - lam) * dl;
+            const f2 w2{w, w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint4 v = ld_chunk(sX, tid, q);
+                const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+                uint32_t out[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const f2 e = ptx::mul2(ptx::bf2_to_f2(in[i]), w2);
+                    out[i] = ptx::f2_to_bf2(e.x, e.y);
+                }
+                st_chunk(sXw, tid, q, make_uint4(out[0], out[1], out[2], out[3]));
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        // ---- (f) Sc = B^T Xw  (rows = states, columns = p)
+        if (tid == 0) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kQ / 16; ++k) {
+                const uint64_t da = ptx::sdesc_sw128(aB + k * 2048, kTile, 1024);
+                const uint64_t db = ptx::sdesc_sw128(aXw + k * 2048, 1024, 1024);
+                ptx::mma_bf16(tmem + kColSc, da, db, id_Sc, k > 0);
+            }
+            ptx::mma_commit(bar_mma);
+        }
+        if (!wait_all(bar_mma, ph_mma)) {
+            ok = false;
+            pending = 2;
+            break;
+        }
+        ph_mma ^= 1;
+        ptx::tc_fence_after();
+
+        // ---- (g) M[t, s] = G[t, s] exp(Lam_t - Lam_s) dl_s for s <= t (row t = tid)
+        {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {   // 32-column groups of s
+                const int kb = i >> 1;
+                if (i <= warp) {           // warp-uniform: some s in the group is <= t
+                    float gv[32];
+                    ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t out[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float m2[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int s = 32 * i + 8 * q + 2 * e + u;
+                                const float val = gv[8 * q + 2 * e + u] *
+                                                  ex2_approx(lam - s_lam[s]) * s_dl[s];
+                                m2[u] = s <= tid ? val : 0.f;
+                            }
+                            out[e] = ptx::f2_to_bf2(m2[0], m2[1]);
+                        }
+                        st_chunk(sM + kb * kTile, tid, (i & 1) * 4 + q,
+                                 make_uint4(out[0], out[1], out[2], out[3]));
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_chunk(sM + kb * kTile, tid, (i & 1) * 4 + q, make_uint4(0, 0, 0, 0));
+                }
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+        // ---- (h) Yd = M X
+        if (tid == 0) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kQ / 16; ++k) {
+                const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
+                const uint64_t da = ptx::sdesc_sw128(aM + off, 16, 1024);
+                const uint64_t db = ptx::sdesc_sw128(aX + k * 2048, 1024, 1024);
+                ptx::mma_bf16(tmem + kColYd, da, db, id_Yd, k > 0);
+            }
+            ptx::mma_commit(bar_mma);
+        }
+        // ---- (i) state: S <- exp(Lam_end) S + Sc (row n = tid), bf16 copy for the next Yo
+        {
+            const float dec = ex2_approx(lam_end);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float sc[32];
+                ptx::tmem_ld32(tmem + lane_base + kColSc + 32 * half, sc);
+#pragma unroll
+                for (int pp = 0; pp < 32; ++pp) S[32 * half + pp] = fmaf(dec, S[32 * half + pp], sc[pp]);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint4 v;
+                v.x = ptx::f2_to_bf2(S[8 * q + 0], S[8 * q + 1]);
+                v.y = ptx::f2_to_bf2(S[8 * q + 2], S[8 * q + 3]);
+                v.z = ptx::f2_to_bf2(S[8 * q + 4], S[8 * q + 5]);
+                v.w = ptx::f2_to_bf2(S[8 * q + 6], S[8 * q + 7]);
+                st_chunk(sS, tid, q, v);
+            }
+        }
+        if (!wait_all(bar_mma, ph_mma)) {
+            ok = false;
+            pending = 2;
+            break;
+        }
+        ph_mma ^= 1;
+        ptx::tc_fence_after();
+        // ---- (j) y = Yd + exp(Lam_t) Yo + D x (x gate), written over X in place
+        {
+            const float et = ex2_approx(lam);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float yd[32], yo[32];
+                ptx::tmem_ld32(tmem + lane_base + kColYd + 32 * half, yd);
+                ptx::tmem_ld32(tmem + lane_base + kColYo + 32 * half, yo);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int qq = half * 4 + q;
+                    const uint4 xv = ld_chunk(sX, tid, qq);
+                    const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
+                    uint32_t zin[4] = {0, 0, 0, 0};
+                    if (kGate) {
+                        const uint4 zv = ld_chunk(sZ, tid, qq);
+                        zin[0] = zv.x; zin[1] = zv.y; zin[2] = zv.z; zin[3] = zv.w;
+                    }
+                    uint32_t out[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const f2 xf = ptx::bf2_to_f2(xin[e]);
+                        const int j = 8 * q + 2 * e;
+                        float y0 = fmaf(et, yo[j], yd[j]);
+                        float y1 = fmaf(et, yo[j + 1], yd[j + 1]);
+                        y0 = fmaf(Dh, xf.x, y0);
+                        y1 = fmaf(Dh, xf.y, y1);
+                        if (kGate) {
+                            const f2 zf = ptx::bf2_to_f2(zin[e]);
+                            y0 *= silu<true>(zf.x);
+                            y1 *= silu<true>(zf.y);
+                        }
+                        out[e] = ptx::f2_to_bf2(y0, y1);
+                    }
+                    st_chunk(sX, tid, qq, make_uint4(out[0], out[1], out[2], out[3]));
+                }
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            ptx::tma_store_3d(&maps.Y, sX, h * kP, t0, b);
+            ptx::bulk_commit();
+        }
+    }
+
+    if (!ok) {
+        if (tid == 0) report_status(status, SSM_ERR_TIMEOUT, 20 + pending);
+        // give the late operation one more bounded wait before TMEM and shared
+        // memory are released
+        if (pending == 1) (void)ptx::mbar_wait(bar_load, ph_load);
+        if (pending == 2) (void)ptx::mbar_wait(bar_mma, ph_mma);
+    }
+    if (tid == 0) ptx::bulk_wait<0>();
+    if (ok && p.h_final) {
+        float *hf = p.h_final + (static_cast<int64_t>(b) * H + h) * kP * kN;
+#pragma unroll
+        for (int pp = 0; pp < kP; ++pp) hf[pp * kN + tid] = S[pp];
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 3-D bf16 map over a (B, L, W) row-major tensor, box (64, 128, 1), 128-byte swizzle.
+bool make_map_sw128(CUtensorMap *m, const void *base, int64_t B, int64_t L, int64_t W) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(L),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(W * 2), static_cast<cuuint64_t>(L * W * 2)};
+    cuuint32_t box[3] = {64, kQ, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool ssd_tc_eligible(const SSDParams &p) {
+    if (!p.io_bf16 || p.headdim != kP || p.dstate != kN) return false;
+    if (p.seqlen <= 0 || p.seqlen >= (int64_t(1) << 31)) return false;
+    if (p.nheads > 65535 || p.batch > 65535) return false;
+    const void *ptrs[] = {p.x, p.Bm, p.Cm, p.z, p.y};
+    for (const void *q : ptrs)
+        if (q && reinterpret_cast<uintptr_t>(q) % 16 != 0) return false;
+    return encoder() != nullptr;
+}
+
+cudaError_t launch_ssd_tc(const SSDParams &p, cudaStream_t stream) {
+    Maps m{};
+    const int64_t B = p.batch, L = p.seqlen, H = p.nheads, G = p.ngroups;
+    bool ok = make_map_sw128(&m.C, p.Cm, B, L, G * kN) && make_map_sw128(&m.B, p.Bm, B, L, G * kN) &&
+              make_map_sw128(&m.X, p.x, B, L, H * kP) && make_map_sw128(&m.Y, p.y, B, L, H * kP);
+    if (ok && p.z) ok = make_map_sw128(&m.Z, p.z, B, L, H * kP);
+    if (!ok) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(B));
+    cudaError_t e;
+    if (p.z) {
+        e = cudaFuncSetAttribute(ssd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
+        ssd_tc_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(m, p);
+    } else {
+        e = cudaFuncSetAttribute(ssd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
+        ssd_tc_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(m, p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ssm

@@ -62,9 +62,12 @@ ssm_status check_scan(const ssm_scan_args *a, bool pointers = true) {
     return SSM_OK;
 }
 
+// The plan depends on sizes and flags only: the TMA-staged kernel's plan when the
+// sizes allow it (pointers that turn out unaligned at call time run the general
+// kernel on the same plan).  The workspace always holds the device status word.
 size_t scan_ws(const ssm_scan_args *a, int64_t *chunk_len, int *nchunks) {
-    ssm::scan_plan(a->batch, a->seqlen, a->dim, a->dstate, a->time_chunk, chunk_len, nchunks);
-    if (*nchunks <= 1) return 0;
+    const bool tma = ssm::scan_tma_sizes_ok(a->io_dtype == SSM_BF16, a->seqlen, a->dim, a->dstate);
+    ssm::scan_plan(a->batch, a->seqlen, a->dim, a->dstate, a->time_chunk, tma, chunk_len, nchunks);
     return ssm::scan_workspace_bytes(a->batch, a->dim, a->dstate, *nchunks);
 }
 
@@ -210,10 +213,10 @@ ssm_status ssm_scan_fwd(const ssm_scan_args *a, ssm_stream_t stream) {
     if (s != SSM_OK) return s;
     int64_t cl;
     int k;
-    const size_t need = scan_ws(a, &cl, &k);
-    if (need > 0 && (!a->workspace || a->workspace_bytes < need)) return SSM_ERR_WORKSPACE;
-    if (need > 0 && !aligned(a->workspace, 256)) return SSM_ERR_ALIGNMENT;
     if (a->batch == 0 || a->dim == 0) return SSM_OK;  // nothing to write
+    const size_t need = scan_ws(a, &cl, &k);
+    if (!a->workspace || a->workspace_bytes < need) return SSM_ERR_WORKSPACE;
+    if (!aligned(a->workspace, 256)) return SSM_ERR_ALIGNMENT;
     ssm::ScanParams p{};
     p.batch = a->batch;
     p.seqlen = a->seqlen;
@@ -234,6 +237,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_args *a, ssm_stream_t stream) {
     p.h_final = a->h_final;
     p.chunk_len = cl;
     p.nchunks = k;
+    p.status = a->workspace;
     if (k > 1) {
         char *ws = static_cast<char *>(a->workspace) + kStatusBytes;
         const size_t rows = (size_t)a->batch * k * a->dim;
@@ -248,6 +252,14 @@ ssm_status ssm_ssd_workspace_size(const ssm_ssd_args *a, size_t *bytes) {
     ssm_status s = check_ssd(a, false);
     if (s != SSM_OK) return s;
     *bytes = ssm::ssd_workspace_bytes(ssd_params(a));
+    return SSM_OK;
+}
+
+ssm_status ssm_ssd_plan(const ssm_ssd_args *a, int32_t *tensor_core) {
+    if (!tensor_core) return SSM_ERR_INVALID_ARG;
+    ssm_status s = check_ssd(a);
+    if (s != SSM_OK) return s;
+    *tensor_core = ssm::ssd_tc_eligible(ssd_params(a)) ? 1 : 0;
     return SSM_OK;
 }
 

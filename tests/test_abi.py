@@ -33,7 +33,7 @@ def header_functions():
 
 def test_header_declares_expected_entry_points():
     fns = header_functions()
-    for name in ("ssm_scan_fwd", "ssm_ssd_chunk_fwd", "ssm_step_decode",
+    for name in ("ssm_scan_fwd", "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_ssd_plan",
                  "ssm_scan_workspace_size", "ssm_ssd_workspace_size", "ssm_status_string",
                  "ssm_version", "ssm_read_device_status"):
         assert name in fns
@@ -106,9 +106,14 @@ def test_scan_plan(lib):
     assert ssm.scan_plan(0, 300, 8, 16)[2] == 0
 
 
-def test_scan_workspace_is_zero_without_time_split(lib):
-    assert ssm.scan_workspace_size(8, 2048, 1536, 16) == 0
-    assert ssm.scan_workspace_size(1, 131072, 2048, 16) > 0
+def test_scan_workspace_holds_status_word_and_chunk_summaries(lib):
+    # one time chunk: only the 256-byte device status word
+    assert ssm.scan_workspace_size(8, 2048, 1536, 16) == 256
+    # the long-context shape is split over time: status word + per-chunk end states
+    cl, k, launches = ssm.scan_plan(1, 131072, 2048, 16)
+    assert k > 1 and launches == 2
+    need = 256 + (1 * k * 2048 * 16 * 4 + 255) // 256 * 256 + (k * 2048 * 4 + 255) // 256 * 256
+    assert ssm.scan_workspace_size(1, 131072, 2048, 16) == need
 
 
 def test_empty_problems_return_without_launch(lib):

@@ -5,7 +5,9 @@ import pytest
 import oracle
 from selective_state_space_132_b300 import workloads as W
 
-from _parity import assert_close, run_scan, run_ssd
+import selective_state_space_132_b300 as ssm
+
+from _parity import assert_close, dev, io_dtype, run_scan, run_ssd
 
 pytestmark = pytest.mark.gpu
 
@@ -24,6 +26,32 @@ def _check(p, chunk=None):
 def test_shapes(io, P, N, G, H):
     p = W.ssd_problem(2, 300, H, P, G, N, chunk=64, io=io, seed=60 + P + N, h0=True)
     _check(p)
+
+
+def _uses_tc(p):
+    io = io_dtype(p.io)
+    return ssm.ssd_uses_tensor_cores(dev(p.x, io), dev(p.delta, io), dev(p.A), dev(p.B, io),
+                                     dev(p.C, io), z=dev(p.z, io))
+
+
+@pytest.mark.parametrize("L,nb,H,G,gate,h0", [(1, 1, 2, 1, False, False),
+                                              (77, 2, 3, 1, True, True),
+                                              (128, 1, 2, 2, False, True),
+                                              (129, 3, 4, 2, False, False),
+                                              (700, 2, 6, 3, True, True)])
+def test_tensor_core_path(L, nb, H, G, gate, h0):
+    """The tcgen05 chunked kernel (bf16, P = 64, N = 128): short, exact-tile, ragged and
+    multi-tile sequences, several batches and groups, with and without gate and h0."""
+    p = W.ssd_problem(nb, L, H, 64, G, 128, chunk=128, io="bf16", seed=80 + L + H, gate=gate,
+                      h0=h0)
+    assert _uses_tc(p)
+    _check(p)
+
+
+def test_tensor_core_path_is_not_taken_for_other_shapes():
+    assert not _uses_tc(W.ssd_problem(1, 64, 2, 32, 1, 128, io="bf16", seed=1))
+    assert not _uses_tc(W.ssd_problem(1, 64, 2, 64, 1, 64, io="bf16", seed=1))
+    assert not _uses_tc(W.ssd_problem(1, 64, 2, 64, 1, 128, io="f32", seed=1))
 
 
 @pytest.mark.parametrize("chunk", [32, 64, 128, 256])
@@ -60,6 +88,7 @@ def test_mamba2_full_size_sampled_heads():
     """Reference workload: batch 4, L 8192, 80 heads x 64, N 128, one group, chunk 256,
     bf16; the GPU runs it in full, the oracle checks 6 sampled (batch, head) pairs."""
     p = W.config_problem(3)
+    assert _uses_tc(p)
     y, hf = run_ssd(p)
     pairs = [(0, 0), (0, 79), (1, 13), (2, 40), (3, 5), (3, 66)]
     for b, h in pairs:
