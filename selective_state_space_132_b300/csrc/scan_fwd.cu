@@ -362,8 +362,8 @@ void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64
         // keep chunks at least 1024 steps long.
         int64_t warps, target;
         if (tma) {
-            const int64_t cpw = 32 / scan_tma_lanes(dstate);
-            warps = batch * ((dim + cpw - 1) / cpw);
+            // blocks of 32 channels with one warp per lane slot of a channel
+            warps = batch * ((dim + 31) / 32) * scan_tma_lanes(dstate);
             target = static_cast<int64_t>(device_sm_count()) * 10;
         } else {
             warps = batch * ((dim + kDT - 1) / kDT) * lanes_for(dstate);

@@ -51,84 +51,91 @@ using ptx::f2;
 
 constexpr int kT = 32;       // time steps per tile (one per lane in prologue/epilogue)
 constexpr int kStages = 2;   // TMA pipeline depth
+#ifndef SSM_SCAN_UNROLL
+#define SSM_SCAN_UNROLL 4
+#endif
+constexpr int kU = SSM_SCAN_UNROLL;  // time steps per ILP block of the scan loop
 
-__host__ __device__ constexpr int align128(int v) { return (v + 127) / 128 * 128; }
+__host__ __device__ constexpr int align1k(int v) { return (v + 1023) / 1024 * 1024; }
 
-template <typename TIO, int NS, int LPC, bool kSummary> struct Layout {
-    static constexpr int CPW = 32 / LPC;  // channels per block
+// Shared-memory layout of one block: WPC warps, each owning CPW = 32 / LPC channels;
+// the block's CPB = WPC * CPW channels form one token-tile row of ROWB bytes.
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary> struct Layout {
+    static constexpr int CPW = 32 / LPC;
+    static constexpr int CPB = CPW * WPC;
     static constexpr int N = NS * LPC;
     static constexpr int E = sizeof(TIO);
-    static constexpr int kTok = kT * CPW * E;  // bytes of one x / delta / z tile
+    static constexpr int ROWB = CPB * E;       // 32, 64 or 128 bytes (swizzle span)
+    static constexpr int kTok = kT * ROWB;     // bytes of one x / delta / z tile
     static constexpr int kBC = kT * N * E;     // bytes of one B or C tile
+    static constexpr bool kConvBC = E != 4;    // bf16 B/C are widened to fp32 once
     // one pipeline stage: x, delta, z, B, C (no z, C in the summary pass)
     static constexpr int s_x = 0;
-    static constexpr int s_dl = s_x + align128(kTok);
-    static constexpr int s_z = s_dl + align128(kTok);
-    static constexpr int s_B = s_z + (kSummary ? 0 : align128(kTok));
-    static constexpr int s_C = s_B + align128(kBC);
-    static constexpr int stage = s_C + (kSummary ? 0 : align128(kBC));
+    static constexpr int s_dl = s_x + align1k(kTok);
+    static constexpr int s_z = s_dl + align1k(kTok);
+    static constexpr int s_B = s_z + (kSummary ? 0 : align1k(kTok));
+    static constexpr int s_C = s_B + align1k(kBC);
+    static constexpr int stage = s_C + (kSummary ? 0 : align1k(kBC));
     // bytes one stage receives (z only when a gate is given)
     __host__ __device__ static constexpr int tx_bytes(bool gate) {
         return (kSummary ? 2 : (gate ? 3 : 2)) * kTok + (kSummary ? 1 : 2) * kBC;
     }
-    // work buffers after the stages
-    static constexpr int kDlxRow = 2 * kT + 4;  // floats per channel row of (dl, dl x)
+    // fp32 (dl, dl x) pairs, one row of 2 kT floats per channel (16-byte aligned rows)
+    static constexpr int kDlxRow = 2 * kT + 4;
     static constexpr int o_dlx = kStages * stage;
-    static constexpr int o_Bf = o_dlx + align128(CPW * kDlxRow * 4);
-    static constexpr int o_Cf = o_Bf + align128(kT * N * 4);
-    // floats per lane slot of the partial readouts; the CPW-float pad puts the
-    // LPC slots of one time step on distinct banks
-    static constexpr int kPart = kT * CPW + CPW;
-    static constexpr int o_part = o_Cf + (kSummary ? 0 : align128(kT * N * 4));
-    static constexpr int o_y = o_part + (kSummary ? 0 : align128(LPC * kPart * 4));
-    static constexpr int o_bar = o_y + (kSummary ? 0 : 2 * align128(kTok));
-    static constexpr int bytes = o_bar + kStages * 8;
+    static constexpr int o_Bf = o_dlx + align1k(CPB * kDlxRow * 4);
+    static constexpr int o_Cf = o_Bf + (kConvBC ? align1k(kT * N * 4) : 0);
+    // per warp: LPC slots of partial readouts [slot][t][channel], t-stride CPW + 4
+    // (conflict-free row reads) and slot stride = 8 mod 32 (conflict-free writes)
+    static constexpr int kPartT = CPW + 4;
+    static constexpr int kPart = (kT * kPartT + 31) / 32 * 32 + 8;
+    static constexpr int o_part = o_Cf + ((kConvBC && !kSummary) ? align1k(kT * N * 4) : 0);
+    static constexpr int o_y = o_part + (kSummary ? 0 : align1k(WPC * LPC * kPart * 4));
+    static constexpr int o_bar = o_y + (kSummary ? 0 : 2 * align1k(kTok));
+    static constexpr int bytes = o_bar + kStages * 8 + 1024;  // + slack to align the base
 };
 
 struct TmaMaps {
     CUtensorMap x, dl, z, B, C, y;
 };
 
-// Element loads of one tile row (CPW consecutive channels) as floats.
-template <typename TIO, int CPW> struct Row;
-template <int CPW> struct Row<float, CPW> {
-    static __device__ __forceinline__ void load(const unsigned char *p, float (&v)[CPW]) {
-#pragma unroll
-        for (int c = 0; c < CPW; c += 4) {
-            const float4 q = *reinterpret_cast<const float4 *>(p + 4 * c);
-            v[c] = q.x; v[c + 1] = q.y; v[c + 2] = q.z; v[c + 3] = q.w;
-        }
+// Byte offset of 16-byte chunk `q` of row `t` in a token tile: the TMA swizzle
+// of a ROWB-byte row (32/64/128-byte mode) XORs the chunk index with address bits 7+.
+template <int ROWB> __device__ __forceinline__ int tok_chunk(int t, int q) {
+    return t * ROWB + ((q ^ ((t * ROWB >> 7) & (ROWB / 16 - 1))) << 4);
+}
+
+// 16-byte chunk of 8 bf16 or 4 fp32 values as floats.
+template <typename TIO> struct Chunk;
+template <> struct Chunk<float> {
+    static constexpr int EC = 4;
+    static __device__ __forceinline__ void load(const unsigned char *p, float (&v)[4]) {
+        const float4 q = *reinterpret_cast<const float4 *>(p);
+        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
     }
-    static __device__ __forceinline__ void store(unsigned char *p, const float (&v)[CPW]) {
-#pragma unroll
-        for (int c = 0; c < CPW; c += 4)
-            *reinterpret_cast<float4 *>(p + 4 * c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+    static __device__ __forceinline__ void store(unsigned char *p, const float (&v)[4]) {
+        *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
     }
 };
-template <int CPW> struct Row<__nv_bfloat16, CPW> {
-    static __device__ __forceinline__ void load(const unsigned char *p, float (&v)[CPW]) {
+template <> struct Chunk<__nv_bfloat16> {
+    static constexpr int EC = 8;
+    static __device__ __forceinline__ void load(const unsigned char *p, float (&v)[8]) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(p);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int c = 0; c < CPW; c += 8) {
-            const uint4 q = *reinterpret_cast<const uint4 *>(p + 2 * c);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const f2 e = ptx::bf2_to_f2(w[i]);
-                v[c + 2 * i] = e.x;
-                v[c + 2 * i + 1] = e.y;
-            }
+        for (int i = 0; i < 4; ++i) {
+            const f2 e = ptx::bf2_to_f2(w[i]);
+            v[2 * i] = e.x;
+            v[2 * i + 1] = e.y;
         }
     }
-    static __device__ __forceinline__ void store(unsigned char *p, const float (&v)[CPW]) {
-#pragma unroll
-        for (int c = 0; c < CPW; c += 8) {
-            uint4 q;
-            q.x = ptx::f2_to_bf2(v[c], v[c + 1]);
-            q.y = ptx::f2_to_bf2(v[c + 2], v[c + 3]);
-            q.z = ptx::f2_to_bf2(v[c + 4], v[c + 5]);
-            q.w = ptx::f2_to_bf2(v[c + 6], v[c + 7]);
-            *reinterpret_cast<uint4 *>(p + 2 * c) = q;
-        }
+    static __device__ __forceinline__ void store(unsigned char *p, const float (&v)[8]) {
+        uint4 q;
+        q.x = ptx::f2_to_bf2(v[0], v[1]);
+        q.y = ptx::f2_to_bf2(v[2], v[3]);
+        q.z = ptx::f2_to_bf2(v[4], v[5]);
+        q.w = ptx::f2_to_bf2(v[6], v[7]);
+        *reinterpret_cast<uint4 *>(p) = q;
     }
 };
 
@@ -139,34 +146,38 @@ template <bool kFast> __device__ __forceinline__ f2 decay2(float dl, f2 a) {
     return f2{expf(v.x), expf(v.y)};
 }
 
-template <typename TIO, int NS, int LPC, bool kSummary>
-__global__ void __launch_bounds__(32) scan_tma_kernel(const __grid_constant__ TmaMaps maps,
-                                                      ScanParams p) {
-    using LY = Layout<TIO, NS, LPC, kSummary>;
-    constexpr int CPW = LY::CPW;
-    constexpr int N = LY::N;
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary>
+__global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constant__ TmaMaps maps,
+                                                            ScanParams p) {
+    using LY = Layout<TIO, NS, LPC, WPC, kSummary>;
+    using CK = Chunk<TIO>;
+    constexpr int CPW = LY::CPW, CPB = LY::CPB, N = LY::N, ROWB = LY::ROWB;
+    constexpr int EC = CK::EC;                  // elements per 16-byte chunk
+    constexpr int QW = CPW / EC;                // chunks of a warp's channels in one row
     constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
-    static_assert(NS % 2 == 0, "states per lane must be even (packed pairs)");
-    static_assert(CPW * sizeof(TIO) % 16 == 0 && N * sizeof(TIO) % 16 == 0, "TMA row sizes");
+    constexpr int NT = 32 * WPC;
+    static_assert(NS % 2 == 0 && CPW % EC == 0, "layout");
+    static_assert(ROWB == 32 || ROWB == 64 || ROWB == 128, "token rows must match a TMA swizzle");
 
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + LY::o_bar);
     float *dlx = reinterpret_cast<float *>(smem + LY::o_dlx);
-    float *Bf = reinterpret_cast<float *>(smem + LY::o_Bf);
-    float *Cf = reinterpret_cast<float *>(smem + LY::o_Cf);
-    float *part = reinterpret_cast<float *>(smem + LY::o_part);
 
-    const int lane = threadIdx.x;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
     const int64_t D = p.dim, L = p.seqlen;
     const int K = p.nchunks;
     const int b = blockIdx.y;
     const int c = blockIdx.z;
-    const int d0 = blockIdx.x * CPW;
+    const int d0 = blockIdx.x * CPB;
     const bool has_z = p.z != nullptr;
     DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
+    float *part = reinterpret_cast<float *>(smem + LY::o_part) + warp * LPC * LY::kPart;
 
     // the first block of the first launch of a call clears the status word
-    if (p.clear_status && status && lane == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
+    if (p.clear_status && status && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
         blockIdx.z == 0)
         status->code = 0;
 
@@ -174,13 +185,13 @@ __global__ void __launch_bounds__(32) scan_tma_kernel(const __grid_constant__ Tm
     const int64_t t_end = min(L, t_begin + p.chunk_len);
     const int ntiles = static_cast<int>((t_end - t_begin + kT - 1) / kT);
 
-    if (lane == 0) {
+    if (tid == 0) {
         for (int s = 0; s < kStages; ++s) ptx::mbar_init(&bars[s], 1);
         ptx::fence_mbar_init();
     }
-    __syncwarp();
+    __syncthreads();
 
-    auto issue = [&](int tile) {  // lane 0 only
+    auto issue = [&](int tile) {  // thread 0 only
         const int s = tile % kStages;
         unsigned char *st = smem + s * LY::stage;
         const int t0 = static_cast<int>(t_begin + static_cast<int64_t>(tile) * kT);
@@ -193,15 +204,15 @@ __global__ void __launch_bounds__(32) scan_tma_kernel(const __grid_constant__ Tm
             ptx::tma_load_3d(st + LY::s_C, &maps.C, &bars[s], 0, t0, b);
         }
     };
-    if (lane == 0) {
+    if (tid == 0) {
         ptx::prefetch_tmap(&maps.x);
         for (int i = 0; i < kStages && i < ntiles; ++i) issue(i);
     }
 
-    // ---------------- per-lane constants
-    // scan role: channel sc, lane slot j owns states j*NS .. j*NS+NS-1
+    // ---------------- per-thread constants
+    // scan role: channel sc of this warp, lane slot j owns states j*NS .. j*NS+NS-1
     const int sc = lane / LPC, j = lane % LPC;
-    const int64_t sd = d0 + sc;
+    const int64_t sd = d0 + warp * CPW + sc;
     const bool sdval = sd < D;
     f2 a2[NS / 2], h[NS / 2];
 #pragma unroll
@@ -224,16 +235,17 @@ __global__ void __launch_bounds__(32) scan_tma_kernel(const __grid_constant__ Tm
 #pragma unroll
             for (int k = 0; k < NS / 2; ++k) {
                 const int n = j * NS + 2 * k;
-                const f2 he = sdval ? f2{p.hloc[row * N + n], p.hloc[row * N + n + 1]} : f2{0.f, 0.f};
+                const f2 he = sdval ? f2{p.hloc[row * N + n], p.hloc[row * N + n + 1]}
+                                    : f2{0.f, 0.f};
                 h[k] = ptx::fma2(decay2<kFast>(S, a2[k]), h[k], he);
             }
         }
     }
-    // prologue / epilogue role: row t = lane of the tile, all CPW channels
+    // prologue / epilogue role: row t = lane, this warp's CPW channels
     float pbias[CPW], pD[CPW];
 #pragma unroll
     for (int cc = 0; cc < CPW; ++cc) {
-        const int64_t d = d0 + cc;
+        const int64_t d = d0 + warp * CPW + cc;
         pbias[cc] = (d < D && p.bias) ? p.bias[d] : 0.f;
         pD[cc] = (!kSummary && d < D && p.Dv) ? p.Dv[d] : 0.f;
     }
@@ -244,131 +256,172 @@ __global__ void __launch_bounds__(32) scan_tma_kernel(const __grid_constant__ Tm
         const int s = tile % kStages;
         const unsigned char *st = smem + s * LY::stage;
         const int64_t t0 = t_begin + static_cast<int64_t>(tile) * kT;
-        if (!ptx::mbar_wait(&bars[s], (tile / kStages) & 1)) {
+        const bool got = ptx::mbar_wait(&bars[s], (tile / kStages) & 1);
+
+        // ---------------- prologue (only after this thread's own wait succeeded)
+        const float *Bf = reinterpret_cast<const float *>(LY::kConvBC ? smem + LY::o_Bf
+                                                                     : st + LY::s_B);
+        const float *Cf = reinterpret_cast<const float *>(LY::kConvBC ? smem + LY::o_Cf
+                                                                     : st + LY::s_C);
+        if (got) {
+            const bool tval = t0 + lane < t_end;
+#pragma unroll
+            for (int q = 0; q < QW; ++q) {
+                const int qc = warp * QW + q;  // chunk index within the row
+                float vd[EC], vx[EC];
+                CK::load(st + LY::s_dl + tok_chunk<ROWB>(lane, qc), vd);
+                CK::load(st + LY::s_x + tok_chunk<ROWB>(lane, qc), vx);
+#pragma unroll
+                for (int e = 0; e < EC; ++e) {
+                    const int cc = q * EC + e;
+                    const float dl = tval ? step_size<kFast>(vd[e], pbias[cc], p.softplus) : 0.f;
+                    *reinterpret_cast<float2 *>(dlx + (warp * CPW + cc) * LY::kDlxRow + 2 * lane) =
+                        make_float2(dl, dl * vx[e]);
+                }
+            }
+            if constexpr (LY::kConvBC) {
+                // B (and C) tiles to fp32, shared by the block: 16-byte chunks
+                constexpr int kChunksBC = LY::kBC / 16;
+                constexpr int kTot = (kSummary ? 1 : 2) * kChunksBC;
+                for (int q = tid; q < kTot; q += NT) {
+                    const bool isC = q >= kChunksBC;
+                    const int qq = isC ? q - kChunksBC : q;
+                    float v[EC];
+                    CK::load(st + (isC ? LY::s_C : LY::s_B) + qq * 16, v);
+                    float *dst = reinterpret_cast<float *>(smem + (isC ? LY::o_Cf : LY::o_Bf)) +
+                                 qq * EC;
+                    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                    *reinterpret_cast<float4 *>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                }
+            }
+        }
+        if (!__syncthreads_and(got ? 1 : 0)) {
             failed_tile = tile;
             break;
         }
-        // ---------------- prologue: row t = lane
-        {
-            const bool tval = t0 + lane < t_end;
-            float vx[CPW], vd[CPW];
-            Row<TIO, CPW>::load(st + LY::s_dl + lane * CPW * sizeof(TIO), vd);
-            Row<TIO, CPW>::load(st + LY::s_x + lane * CPW * sizeof(TIO), vx);
-#pragma unroll
-            for (int cc = 0; cc < CPW; ++cc) {
-                const float dl = tval ? step_size<kFast>(vd[cc], pbias[cc], p.softplus) : 0.f;
-                *reinterpret_cast<float2 *>(dlx + cc * LY::kDlxRow + 2 * lane) =
-                    make_float2(dl, dl * vx[cc]);
-            }
-            // B (and C) row t to fp32
-            float vb[N];
-            Row<TIO, N>::load(st + LY::s_B + lane * N * sizeof(TIO), vb);
-            Row<float, N>::store(reinterpret_cast<unsigned char *>(Bf + lane * N), vb);
-            if (!kSummary) {
-                Row<TIO, N>::load(st + LY::s_C + lane * N * sizeof(TIO), vb);
-                Row<float, N>::store(reinterpret_cast<unsigned char *>(Cf + lane * N), vb);
-            }
-        }
-        __syncwarp();
 
-        // ---------------- scan: NS states per lane, in time order
+        // ---------------- scan: NS states per lane, in time order, kU steps per block
         {
-            const float *row = dlx + sc * LY::kDlxRow;
-#pragma unroll 4
-            for (int tt = 0; tt < kT; tt += 2) {
-                const float4 q = *reinterpret_cast<const float4 *>(row + 2 * tt);
+            const float *row = dlx + (warp * CPW + sc) * LY::kDlxRow;
+#pragma unroll 2
+            for (int tb = 0; tb < kT; tb += kU) {
+                float dl[kU], dx[kU];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const float dl = i ? q.z : q.x;
-                    const float dx = i ? q.w : q.y;
-                    const float *Bt = Bf + (tt + i) * N + j * NS;
-                    const float *Ct = Cf + (tt + i) * N + j * NS;
-                    f2 acc{0.f, 0.f};
-                    f2 bp[NS / 2], cp[NS / 2];
-                    if constexpr (NS % 4 == 0) {
+                for (int u = 0; u < kU; u += 2) {
+                    const float4 q = *reinterpret_cast<const float4 *>(row + 2 * (tb + u));
+                    dl[u] = q.x; dx[u] = q.y; dl[u + 1] = q.z; dx[u + 1] = q.w;
+                }
+                f2 bp[kU][NS / 2], cp[kU][NS / 2];
 #pragma unroll
-                        for (int k = 0; k < NS / 2; k += 2) {
+                for (int u = 0; u < kU; ++u) {
+                    const float *Bt = Bf + (tb + u) * N + j * NS;
+                    const float *Ct = Cf + (tb + u) * N + j * NS;
+#pragma unroll
+                    for (int k = 0; k < NS / 2; k += 2) {
+                        if (k + 1 < NS / 2) {
                             const float4 bq = *reinterpret_cast<const float4 *>(Bt + 2 * k);
-                            bp[k] = f2{bq.x, bq.y};
-                            bp[k + 1 < NS / 2 ? k + 1 : k] = f2{bq.z, bq.w};
+                            bp[u][k] = f2{bq.x, bq.y};
+                            bp[u][k + 1] = f2{bq.z, bq.w};
                             if (!kSummary) {
                                 const float4 cq = *reinterpret_cast<const float4 *>(Ct + 2 * k);
-                                cp[k] = f2{cq.x, cq.y};
-                                cp[k + 1 < NS / 2 ? k + 1 : k] = f2{cq.z, cq.w};
+                                cp[u][k] = f2{cq.x, cq.y};
+                                cp[u][k + 1] = f2{cq.z, cq.w};
                             }
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < NS / 2; ++k) {
+                        } else {
                             const float2 bq = *reinterpret_cast<const float2 *>(Bt + 2 * k);
-                            bp[k] = f2{bq.x, bq.y};
+                            bp[u][k] = f2{bq.x, bq.y};
                             if (!kSummary) {
                                 const float2 cq = *reinterpret_cast<const float2 *>(Ct + 2 * k);
-                                cp[k] = f2{cq.x, cq.y};
+                                cp[u][k] = f2{cq.x, cq.y};
                             }
                         }
                     }
+                }
+                f2 av[kU][NS / 2], uv[kU][NS / 2];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
 #pragma unroll
                     for (int k = 0; k < NS / 2; ++k) {
-                        const f2 a = decay2<kFast>(dl, a2[k]);
-                        const f2 u = ptx::mul2(f2{dx, dx}, bp[k]);
-                        h[k] = ptx::fma2(a, h[k], u);
-                        if (!kSummary) acc = ptx::fma2(cp[k], h[k], acc);
+                        av[u][k] = decay2<kFast>(dl[u], a2[k]);
+                        uv[u][k] = ptx::mul2(f2{dx[u], dx[u]}, bp[u][k]);
                     }
-                    if (!kSummary) part[j * LY::kPart + (tt + i) * CPW + sc] = acc.x + acc.y;
-                    if (kSummary) dsum += dl;
+                }
+                float acc[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    f2 s2{0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < NS / 2; ++k) {
+                        h[k] = ptx::fma2(av[u][k], h[k], uv[u][k]);
+                        if (!kSummary) s2 = ptx::fma2(cp[u][k], h[k], s2);
+                    }
+                    acc[u] = s2.x + s2.y;
+                    if (kSummary) dsum += dl[u];
+                }
+                if (!kSummary) {
+#pragma unroll
+                    for (int u = 0; u < kU; ++u)
+                        part[j * LY::kPart + (tb + u) * LY::kPartT + sc] = acc[u];
                 }
             }
         }
         __syncwarp();
 
-        // ---------------- epilogue: row t = lane
+        // ---------------- epilogue: row t = lane, this warp's channels
         if (!kSummary) {
-            const int yb = tile & 1;
-            unsigned char *ytile = smem + LY::o_y + yb * align128(LY::kTok);
-            if (lane == 0) ptx::bulk_wait_read<1>();  // the store that last used this buffer
-            __syncwarp();
-            float acc[CPW], vx[CPW], vz[CPW];
+            unsigned char *ytile = smem + LY::o_y + (tile & 1) * align1k(LY::kTok);
+            float acc[CPW];
 #pragma unroll
             for (int cc = 0; cc < CPW; cc += 4) {
-                float4 a4 = *reinterpret_cast<const float4 *>(part + lane * CPW + cc);
+                float4 a4 = *reinterpret_cast<const float4 *>(part + lane * LY::kPartT + cc);
 #pragma unroll
                 for (int jj = 1; jj < LPC; ++jj) {
-                    const float4 v = *reinterpret_cast<const float4 *>(part + jj * LY::kPart +
-                                                                       lane * CPW + cc);
-                    a4.x += v.x; a4.y += v.y; a4.z += v.z; a4.w += v.w;
+                    const float4 v = *reinterpret_cast<const float4 *>(
+                        part + jj * LY::kPart + lane * LY::kPartT + cc);
+                    const f2 lo = ptx::add2(f2{a4.x, a4.y}, f2{v.x, v.y});
+                    const f2 hi = ptx::add2(f2{a4.z, a4.w}, f2{v.z, v.w});
+                    a4 = make_float4(lo.x, lo.y, hi.x, hi.y);
                 }
                 acc[cc] = a4.x; acc[cc + 1] = a4.y; acc[cc + 2] = a4.z; acc[cc + 3] = a4.w;
             }
-            Row<TIO, CPW>::load(st + LY::s_x + lane * CPW * sizeof(TIO), vx);
-            if (has_z) Row<TIO, CPW>::load(st + LY::s_z + lane * CPW * sizeof(TIO), vz);
 #pragma unroll
-            for (int cc = 0; cc < CPW; ++cc) {
-                float out = fmaf(pD[cc], vx[cc], acc[cc]);
-                if (has_z) out *= silu<kFast>(vz[cc]);
-                acc[cc] = out;
+            for (int q = 0; q < QW; ++q) {
+                const int qc = warp * QW + q;
+                float vx[EC], vz[EC], out[EC];
+                CK::load(st + LY::s_x + tok_chunk<ROWB>(lane, qc), vx);
+                if (has_z) CK::load(st + LY::s_z + tok_chunk<ROWB>(lane, qc), vz);
+#pragma unroll
+                for (int e = 0; e < EC; ++e) {
+                    const int cc = q * EC + e;
+                    float o = fmaf(pD[cc], vx[e], acc[cc]);
+                    if (has_z) o *= silu<kFast>(vz[e]);
+                    out[e] = o;
+                }
+                CK::store(ytile + tok_chunk<ROWB>(lane, qc), out);
             }
-            Row<TIO, CPW>::store(ytile + lane * CPW * sizeof(TIO), acc);
             ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                ptx::tma_store_3d(&maps.y, ytile, d0, static_cast<int>(t0), b);
-                ptx::bulk_commit();
-            }
         }
-        __syncwarp();
-        // refill this stage with the tile kStages ahead
-        if (lane == 0 && tile + kStages < ntiles) issue(tile + kStages);
+        __syncthreads();
+        if (tid == 0) {
+            if (!kSummary) {
+                ptx::tma_store_3d(&maps.y, smem + LY::o_y + (tile & 1) * align1k(LY::kTok), d0,
+                                  static_cast<int>(t0), b);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read<1>();  // the y tile the next tile writes is free again
+            }
+            // refill this stage with the tile kStages ahead
+            if (tile + kStages < ntiles) issue(tile + kStages);
+        }
     }
 
     if (failed_tile >= 0) {
-        if (lane == 0) report_status(status, SSM_ERR_TIMEOUT, kSummary ? 11 : 12);
+        if (tid == 0) report_status(status, SSM_ERR_TIMEOUT, kSummary ? 11 : 12);
         // let the copies still in flight land before the block's shared memory is
         // released (each wait again bounded)
         for (int i = failed_tile; i < failed_tile + kStages && i < ntiles; ++i)
             if (!ptx::mbar_wait(&bars[i % kStages], (i / kStages) & 1)) break;
     }
-    if (!kSummary && lane == 0) ptx::bulk_wait<0>();
+    if (!kSummary && tid == 0) ptx::bulk_wait<0>();
 
     if (kSummary) {
         const int64_t row = (static_cast<int64_t>(b) * K + c) * D + sd;
@@ -406,9 +459,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
-// 3-D map over a (B, L, W) row-major tensor, box (bw, bt, 1).
+// 3-D map over a (B, L, W) row-major tensor, box (bw, bt, 1); `swizzle_bytes` 0, 32,
+// 64 or 128 selects the shared-memory swizzle of the box rows.
 bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t B, int64_t L, int64_t W,
-              int bw, int bt) {
+              int bw, int bt, int swizzle_bytes) {
     auto enc = encoder();
     if (!enc) return false;
     const size_t e = bf16 ? 2 : 4;
@@ -417,49 +471,55 @@ bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t B, int64_t L,
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(W * e), static_cast<cuuint64_t>(L * W * e)};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(bw), static_cast<cuuint32_t>(bt), 1};
     cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
     CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                      3, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-template <typename TIO, int NS, int LPC, bool kSummary>
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary>
 cudaError_t launch_tma_one(const ScanParams &p, const TmaMaps &maps, int nchunks_grid,
                            cudaStream_t stream) {
-    using LY = Layout<TIO, NS, LPC, kSummary>;
-    auto kern = scan_tma_kernel<TIO, NS, LPC, kSummary>;
+    using LY = Layout<TIO, NS, LPC, WPC, kSummary>;
+    auto kern = scan_tma_kernel<TIO, NS, LPC, WPC, kSummary>;
     if (LY::bytes > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              LY::bytes);
         if (e != cudaSuccess) return e;
     }
-    dim3 grid(static_cast<unsigned>((p.dim + LY::CPW - 1) / LY::CPW),
+    dim3 grid(static_cast<unsigned>((p.dim + LY::CPB - 1) / LY::CPB),
               static_cast<unsigned>(p.batch), static_cast<unsigned>(nchunks_grid));
-    kern<<<grid, 32, LY::bytes, stream>>>(maps, p);
+    kern<<<grid, 32 * WPC, LY::bytes, stream>>>(maps, p);
     return cudaGetLastError();
 }
 
+// Blocks of 32 channels: WPC = LPC warps of 32 / LPC channels each.
 template <typename TIO, int NS, int LPC>
 cudaError_t launch_tma_pair(ScanParams p, cudaStream_t stream) {
-    using LY = Layout<TIO, NS, LPC, false>;
+    constexpr int WPC = LPC;
+    using LY = Layout<TIO, NS, LPC, WPC, false>;
     const bool bf = std::is_same<TIO, __nv_bfloat16>::value;
     TmaMaps m{};
     const int64_t B = p.batch, L = p.seqlen, D = p.dim, N = p.dstate;
-    bool ok = make_map(&m.x, p.x, bf, B, L, D, LY::CPW, kT) &&
-              make_map(&m.dl, p.delta, bf, B, L, D, LY::CPW, kT) &&
-              make_map(&m.B, p.Bm, bf, B, L, N, static_cast<int>(N), kT) &&
-              make_map(&m.C, p.Cm, bf, B, L, N, static_cast<int>(N), kT) &&
-              make_map(&m.y, p.y, bf, B, L, D, LY::CPW, kT);
-    if (ok && p.z) ok = make_map(&m.z, p.z, bf, B, L, D, LY::CPW, kT);
+    bool ok = make_map(&m.x, p.x, bf, B, L, D, LY::CPB, kT, LY::ROWB) &&
+              make_map(&m.dl, p.delta, bf, B, L, D, LY::CPB, kT, LY::ROWB) &&
+              make_map(&m.B, p.Bm, bf, B, L, N, static_cast<int>(N), kT, 0) &&
+              make_map(&m.C, p.Cm, bf, B, L, N, static_cast<int>(N), kT, 0) &&
+              make_map(&m.y, p.y, bf, B, L, D, LY::CPB, kT, LY::ROWB);
+    if (ok && p.z) ok = make_map(&m.z, p.z, bf, B, L, D, LY::CPB, kT, LY::ROWB);
     if (!ok) return cudaErrorInvalidValue;
     p.clear_status = 1;
     if (p.nchunks > 1) {
-        cudaError_t e = launch_tma_one<TIO, NS, LPC, true>(p, m, p.nchunks - 1, stream);
+        cudaError_t e = launch_tma_one<TIO, NS, LPC, WPC, true>(p, m, p.nchunks - 1, stream);
         if (e != cudaSuccess) return e;
         p.clear_status = 0;
     }
-    return launch_tma_one<TIO, NS, LPC, false>(p, m, p.nchunks, stream);
+    return launch_tma_one<TIO, NS, LPC, WPC, false>(p, m, p.nchunks, stream);
 }
 
 }  // namespace
@@ -481,7 +541,6 @@ bool scan_tma_sizes_ok(int io_bf16, int64_t seqlen, int64_t dim, int64_t dstate)
     if (lpc == 0) return false;
     if (io_bf16 && dstate == 4) return false;  // 8-byte B/C rows are below the TMA minimum
     if (dstate * e % 16 != 0 || dim * e % 16 != 0) return false;
-    if ((32 / lpc) * e % 16 != 0) return false;
     return seqlen > 0 && seqlen < (int64_t(1) << 31) && dim < (int64_t(1) << 31);
 }
 
