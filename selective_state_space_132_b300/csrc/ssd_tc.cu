@@ -27,11 +27,16 @@
 //       G  = C B^T        (M=128, N=128, K=N)   A=C  K-major, B=B  K-major
 //       Yo = C S_in^T     (M=128, N=P,   K=N)   A=C  K-major, B=S  MN-major
 //       Sc = B^T Xw       (M=N=128, N=P, K=Q)   A=B  MN-major, B=Xw MN-major
-//       Yd = M X          (M=128, N=P,   K=Q)   A=M  K-major, B=X  MN-major
-//   * CUDA cores build Xw and M (masked exponentials, bf16) straight into shared
-//     memory in the swizzled layout, update the fp32 state held in registers
-//     (thread n owns row n of S^T) and finish y = Yd + exp(Lam_t) Yo + D x, which
-//     goes back to HBM through a TMA store.
+//       Yd = M X          (M=128, N=P,   K=Q)   A=M  in TMEM,  B=X  MN-major
+//   * CUDA cores build Xw (bf16, swizzled shared memory) and M (bf16 pairs written
+//     to TMEM with tcgen05.st; pairwise exponentials on the diagonal 32 x 32 blocks,
+//     a product of two factors <= 1 below them), update the fp32 state held in
+//     registers (thread n owns row n of S^T) and finish y = Yd + exp(Lam_t) Yo + D x,
+//     which goes back to HBM through a TMA store.
+// Two blocks share an SM: TMEM is cut to 256 columns by writing M (bf16 pairs) over
+// the G accumulator and reading it as the A operand of the M X product straight from
+// tensor memory, and shared memory stays under half of the SM by letting the bf16
+// state tile and Xw take turns in one buffer.
 // Shape rules of this kernel: bf16 I/O, P = 64, N = 128; other shapes run the
 // sequential kernel (ssd_chunk.cu).
 #include <cudaTypedefs.h>
@@ -50,25 +55,27 @@ constexpr int kQ = 128;   // chunk length (MMA M)
 constexpr int kP = 64;    // head dim
 constexpr int kN = 128;   // state size
 constexpr int kThreads = 128;
-constexpr int kTmemCols = 512;
-// TMEM column offsets of the accumulators
-constexpr uint32_t kColG = 0, kColYd = 128, kColYo = 192, kColSc = 256;
+constexpr int kTmemCols = 256;  // two blocks per SM share the 512 columns
+// TMEM columns: G (fp32, 128) whose first 64 columns are then overwritten by M
+// (bf16 pairs) and whose last 64 by the chunk state Sc; Yd and Yo (fp32, 64 each).
+constexpr uint32_t kColG = 0, kColM = 0, kColSc = 64, kColYd = 128, kColYo = 192;
 
 // Shared-memory layout (bytes); every operand tile starts on a 1024-byte boundary.
 constexpr int kTile = kQ * 128;                 // 128 rows x 128 bytes = 16 KB
 constexpr int o_C = 0;                          // 2 k-blocks of 64 states
 constexpr int o_B = o_C + 2 * kTile;
 constexpr int o_X = o_B + 2 * kTile;            // also the y staging tile
-constexpr int o_Z = o_X + kTile;
-constexpr int o_M = o_Z + kTile;                // 2 k-blocks of 64 steps
-constexpr int o_Xw = o_M + 2 * kTile;
-constexpr int o_S = o_Xw + kTile;               // S_in^T: 128 state rows x 64 p
-constexpr int o_dl = o_S + kTile;               // float[128]
-constexpr int o_lam = o_dl + kQ * 4;            // float[128]
-constexpr int o_red = o_lam + kQ * 4;           // float[4] warp totals
-constexpr int o_bar = o_red + 64;               // 2 mbarriers
-constexpr int o_tmem = o_bar + 16;
-constexpr int kSmemBytes = o_tmem + 16 + 1024;  // + slack to align the base to 1024
+constexpr int o_W = o_X + kTile;                // S_in^T (bf16) and, once Yo is done, Xw
+constexpr int o_Z = o_W + kTile;                // gate input (only with a gate)
+template <bool kGate> struct Smem {
+    static constexpr int o_dl = o_Z + (kGate ? kTile : 0);  // float[128]
+    static constexpr int o_lam = o_dl + kQ * 4;             // float[128]
+    static constexpr int o_v = o_lam + kQ * 4;              // float[128] column factors
+    static constexpr int o_red = o_v + kQ * 4;              // float[4] warp totals
+    static constexpr int o_bar = o_red + 16;                // 2 mbarriers
+    static constexpr int o_tmem = o_bar + 16;
+    static constexpr int bytes = o_tmem + 16;
+};
 
 struct Maps {
     CUtensorMap C, B, X, Z, Y;
@@ -82,21 +89,25 @@ __device__ __forceinline__ uint4 ld_chunk(const unsigned char *tile, uint32_t ro
 __device__ __forceinline__ void st_chunk(unsigned char *tile, uint32_t row, uint32_t chunk, uint4 v) {
     *reinterpret_cast<uint4 *>(tile + row * 128u + ((chunk ^ (row & 7u)) << 4)) = v;
 }
+__device__ __forceinline__ uint4 pack8(const float *v) {
+    return make_uint4(ptx::f2_to_bf2(v[0], v[1]), ptx::f2_to_bf2(v[2], v[3]),
+                      ptx::f2_to_bf2(v[4], v[5]), ptx::f2_to_bf2(v[6], v[7]));
+}
 
 template <bool kGate>
-__global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_constant__ Maps maps,
+__global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_constant__ Maps maps,
                                                              SSDParams p) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char *sC = smem + o_C, *sB = smem + o_B, *sX = smem + o_X, *sZ = smem + o_Z;
-    unsigned char *sM = smem + o_M, *sXw = smem + o_Xw, *sS = smem + o_S;
-    float *s_dl = reinterpret_cast<float *>(smem + o_dl);
-    float *s_lam = reinterpret_cast<float *>(smem + o_lam);
-    float *s_red = reinterpret_cast<float *>(smem + o_red);
-    uint64_t *bar_load = reinterpret_cast<uint64_t *>(smem + o_bar);
+    using SM = Smem<kGate>;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char *sC = smem + o_C, *sB = smem + o_B, *sX = smem + o_X, *sW = smem + o_W;
+    unsigned char *sZ = smem + o_Z;
+    float *s_dl = reinterpret_cast<float *>(smem + SM::o_dl);
+    float *s_lam = reinterpret_cast<float *>(smem + SM::o_lam);
+    float *s_v = reinterpret_cast<float *>(smem + SM::o_v);
+    float *s_red = reinterpret_cast<float *>(smem + SM::o_red);
+    uint64_t *bar_load = reinterpret_cast<uint64_t *>(smem + SM::o_bar);
     uint64_t *bar_mma = bar_load + 1;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + o_tmem);
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + SM::o_tmem);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -105,6 +116,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
     const int g = static_cast<int>(h / (H / p.ngroups));
     const __nv_bfloat16 *gdt = static_cast<const __nv_bfloat16 *>(p.delta);
     DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
+
+    // The swizzled operand tiles need a 1024-byte aligned base.
+    if (ptx::smem_u32(smem) & 1023u) {
+        if (tid == 0) report_status(status, SSM_ERR_UNSUPPORTED, 29);
+        return;
+    }
 
     const float a_l2 = p.A[h] * kLog2e;  // decay exponent per unit step, base 2
     const float bias = p.bias ? p.bias[h] : 0.f;
@@ -125,30 +142,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
     const uint32_t tmem = *s_tmem;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
 
-    // fp32 state, row n = tid of S^T: S[p][n] for p = 0..63
+    // fp32 state, row n = tid of S^T: S[p][n] for p = 0..63; bf16 copy in sW
     float S[kP];
     {
         const float *h0 = p.h0 ? p.h0 + (static_cast<int64_t>(b) * H + h) * kP * kN : nullptr;
 #pragma unroll
         for (int pp = 0; pp < kP; ++pp) S[pp] = h0 ? h0[pp * kN + tid] : 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            uint4 v;
-            v.x = ptx::f2_to_bf2(S[8 * q + 0], S[8 * q + 1]);
-            v.y = ptx::f2_to_bf2(S[8 * q + 2], S[8 * q + 3]);
-            v.z = ptx::f2_to_bf2(S[8 * q + 4], S[8 * q + 5]);
-            v.w = ptx::f2_to_bf2(S[8 * q + 6], S[8 * q + 7]);
-            st_chunk(sS, tid, q, v);
-        }
+        for (int q = 0; q < 8; ++q) st_chunk(sW, tid, q, pack8(S + 8 * q));
     }
-    ptx::fence_proxy_async_smem();  // the first Yo MMA reads sS
+    ptx::fence_proxy_async_smem();  // the first Yo MMA reads sW
 
     const uint32_t id_G = ptx::idesc_bf16(128, 128, 0, 0);
     const uint32_t id_Yo = ptx::idesc_bf16(128, kP, 0, 1);
     const uint32_t id_Sc = ptx::idesc_bf16(128, kP, 1, 1);
     const uint32_t id_Yd = ptx::idesc_bf16(128, kP, 0, 1);
     const uint32_t aC = ptx::smem_u32(sC), aB = ptx::smem_u32(sB), aX = ptx::smem_u32(sX);
-    const uint32_t aM = ptx::smem_u32(sM), aXw = ptx::smem_u32(sXw), aS = ptx::smem_u32(sS);
+    const uint32_t aW = ptx::smem_u32(sW);
     constexpr uint32_t kLoadBytes = 4 * kTile + (kGate ? 2 : 1) * kTile;
 
     uint32_t ph_load = 0, ph_mma = 0;
@@ -161,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
     };
     const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
 
-    for (int c = 0; c < nchunks && ok; ++c) {
+    for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kQ;
         // ---- (a) loads of this chunk (the previous chunk released every tile)
         if (tid == 0) {
@@ -174,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
             ptx::tma_load_3d(sX, &maps.X, bar_load, h * kP, t0, b);
             if (kGate) ptx::tma_load_3d(sZ, &maps.Z, bar_load, h * kP, t0, b);
         }
-        // ---- (b) step sizes and the running log2-decay
+        // ---- (b) step sizes, the running log2-decay and the column factors
         const int64_t t = t0 + tid;
         float dl = 0.f;
         if (t < L) {
@@ -187,13 +197,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
             const float v = __shfl_up_sync(0xffffffffu, lam, off);
             if (lane >= off) lam += v;
         }
+        // lam of the last step of this warp's 32-step block (before adding earlier warps)
+        const float lam_blk = __shfl_sync(0xffffffffu, lam, 31);
         if (lane == 31) s_red[warp] = lam;
         __syncthreads();
-        for (int w = 0; w < warp; ++w) lam += s_red[w];
+        float base = 0.f;
+        for (int w = 0; w < warp; ++w) base += s_red[w];
+        lam += base;
+        // v_s = exp(Lam_e - Lam_s) dl_s with e the last step of the block holding s
+        s_v[tid] = ex2_approx((base + lam_blk) - lam) * dl;
         s_dl[tid] = dl;
         s_lam[tid] = lam;
-        __syncthreads();
-        const float lam_end = s_lam[kQ - 1];
 
         if (!wait_all(bar_load, ph_load)) {
             ok = false;
@@ -201,8 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
             break;
         }
         ph_load ^= 1;
+        const float lam_tot = s_red[0] + s_red[1] + s_red[2] + s_red[3];
 
-        // ---- (d) G = C B^T and Yo = C S_in^T
+        // ---- (c) G = C B^T and Yo = C S_in^T
         if (tid == 0) {
             ptx::tc_fence_after();
 #pragma unroll
@@ -216,37 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
             for (int k = 0; k < kN / 16; ++k) {
                 const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
                 const uint64_t da = ptx::sdesc_sw128(aC + off, 16, 1024);
-                const uint64_t db = ptx::sdesc_sw128(aS + k * 2048, 1024, 1024);
+                const uint64_t db = ptx::sdesc_sw128(aW + k * 2048, 1024, 1024);
                 ptx::mma_bf16(tmem + kColYo, da, db, id_Yo, k > 0);
-            }
-        }
-        // ---- (e) Xw[s, :] = exp(Lam_end - Lam_s) dl_s x_s  (row s = tid)
-        {
-            const float w = ex2_approx(lam_end - lam) * dl;
-            const f2 w2{w, w};
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint4 v = ld_chunk(sX, tid, q);
-                const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-                uint32_t out[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const f2 e = ptx::mul2(ptx::bf2_to_f2(in[i]), w2);
-                    out[i] = ptx::f2_to_bf2(e.x, e.y);
-                }
-                st_chunk(sXw, tid, q, make_uint4(out[0], out[1], out[2], out[3]));
-            }
-        }
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
-        // ---- (f) Sc = B^T Xw  (rows = states, columns = p)
-        if (tid == 0) {
-            ptx::tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < kQ / 16; ++k) {
-                const uint64_t da = ptx::sdesc_sw128(aB + k * 2048, kTile, 1024);
-                const uint64_t db = ptx::sdesc_sw128(aXw + k * 2048, 1024, 1024);
-                ptx::mma_bf16(tmem + kColSc, da, db, id_Sc, k > 0);
             }
             ptx::mma_commit(bar_mma);
         }
@@ -258,73 +244,80 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
         ph_mma ^= 1;
         ptx::tc_fence_after();
 
-        // ---- (g) M[t, s] = G[t, s] exp(Lam_t - Lam_s) dl_s for s <= t (row t = tid)
+        // ---- (d) Xw[s, :] = exp(Lam_end - Lam_s) dl_s x_s into sW (S_in is consumed)
         {
+            const float w = ex2_approx(lam_tot - lam) * dl;
+            const f2 w2{w, w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {   // 32-column groups of s
-                const int kb = i >> 1;
-                if (i <= warp) {           // warp-uniform: some s in the group is <= t
-                    float gv[32];
-                    ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
+            for (int q = 0; q < 8; ++q) {
+                const uint4 v = ld_chunk(sX, tid, q);
+                const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+                uint32_t out[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t out[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float m2[2];
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int s = 32 * i + 8 * q + 2 * e + u;
-                                const float val = gv[8 * q + 2 * e + u] *
-                                                  ex2_approx(lam - s_lam[s]) * s_dl[s];
-                                m2[u] = s <= tid ? val : 0.f;
-                            }
-                            out[e] = ptx::f2_to_bf2(m2[0], m2[1]);
-                        }
-                        st_chunk(sM + kb * kTile, tid, (i & 1) * 4 + q,
-                                 make_uint4(out[0], out[1], out[2], out[3]));
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        st_chunk(sM + kb * kTile, tid, (i & 1) * 4 + q, make_uint4(0, 0, 0, 0));
+                for (int i = 0; i < 4; ++i) {
+                    const f2 e = ptx::mul2(ptx::bf2_to_f2(in[i]), w2);
+                    out[i] = ptx::f2_to_bf2(e.x, e.y);
                 }
+                st_chunk(sW, tid, q, make_uint4(out[0], out[1], out[2], out[3]));
             }
         }
+        // ---- (e) M[t, s] = G[t, s] exp(Lam_t - Lam_s) dl_s, s <= t, as bf16 pairs over
+        //      G's first 64 columns (row t = tid).  Blocks of 32 columns: below the
+        //      diagonal block exp(Lam_t - Lam_s) = u_t v_s / dl_s with
+        //      u_t = exp(Lam_t - Lam_e), both factors <= 1; on it, pairwise exponentials.
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t packed[16];
+            if (i < warp) {
+                float gv[32];
+                ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
+                const float u = ex2_approx(lam - s_lam[32 * i + 31]);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float2 vv = *reinterpret_cast<const float2 *>(s_v + 32 * i + 2 * e);
+                    const f2 m = ptx::mul2(ptx::mul2(f2{gv[2 * e], gv[2 * e + 1]}, f2{u, u}),
+                                           f2{vv.x, vv.y});
+                    packed[e] = ptx::f2_to_bf2(m.x, m.y);
+                }
+            } else if (i == warp) {
+                float gv[32];
+                ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float m2[2];
+#pragma unroll
+                    for (int u2 = 0; u2 < 2; ++u2) {
+                        const int s = 32 * i + 2 * e + u2;
+                        const float val = gv[2 * e + u2] * ex2_approx(lam - s_lam[s]) * s_dl[s];
+                        m2[u2] = s <= tid ? val : 0.f;
+                    }
+                    packed[e] = ptx::f2_to_bf2(m2[0], m2[1]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) packed[e] = 0u;
+            }
+            ptx::tmem_st16(tmem + lane_base + kColM + 16 * i, packed);
+        }
+        ptx::tmem_wait_st();
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
-        // ---- (h) Yd = M X
+        // ---- (f) Yd = M X (A from TMEM) and Sc = B^T Xw
         if (tid == 0) {
             ptx::tc_fence_after();
 #pragma unroll
             for (int k = 0; k < kQ / 16; ++k) {
-                const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
-                const uint64_t da = ptx::sdesc_sw128(aM + off, 16, 1024);
                 const uint64_t db = ptx::sdesc_sw128(aX + k * 2048, 1024, 1024);
-                ptx::mma_bf16(tmem + kColYd, da, db, id_Yd, k > 0);
+                ptx::mma_bf16_ts(tmem + kColYd, tmem + kColM + 8 * k, db, id_Yd, k > 0);
+            }
+#pragma unroll
+            for (int k = 0; k < kQ / 16; ++k) {
+                const uint64_t da = ptx::sdesc_sw128(aB + k * 2048, kTile, 1024);
+                const uint64_t db = ptx::sdesc_sw128(aW + k * 2048, 1024, 1024);
+                ptx::mma_bf16(tmem + kColSc, da, db, id_Sc, k > 0);
             }
             ptx::mma_commit(bar_mma);
-        }
-        // ---- (i) state: S <- exp(Lam_end) S + Sc (row n = tid), bf16 copy for the next Yo
-        {
-            const float dec = ex2_approx(lam_end);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float sc[32];
-                ptx::tmem_ld32(tmem + lane_base + kColSc + 32 * half, sc);
-#pragma unroll
-                for (int pp = 0; pp < 32; ++pp) S[32 * half + pp] = fmaf(dec, S[32 * half + pp], sc[pp]);
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint4 v;
-                v.x = ptx::f2_to_bf2(S[8 * q + 0], S[8 * q + 1]);
-                v.y = ptx::f2_to_bf2(S[8 * q + 2], S[8 * q + 3]);
-                v.z = ptx::f2_to_bf2(S[8 * q + 4], S[8 * q + 5]);
-                v.w = ptx::f2_to_bf2(S[8 * q + 6], S[8 * q + 7]);
-                st_chunk(sS, tid, q, v);
-            }
         }
         if (!wait_all(bar_mma, ph_mma)) {
             ok = false;
@@ -333,7 +326,21 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
         }
         ph_mma ^= 1;
         ptx::tc_fence_after();
-        // ---- (j) y = Yd + exp(Lam_t) Yo + D x (x gate), written over X in place
+        // ---- (g) state: S <- exp(Lam_end) S + Sc (row n = tid), bf16 copy into sW
+        {
+            const float dec = ex2_approx(lam_tot);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float sc[32];
+                ptx::tmem_ld32(tmem + lane_base + kColSc + 32 * half, sc);
+#pragma unroll
+                for (int pp = 0; pp < 32; ++pp)
+                    S[32 * half + pp] = fmaf(dec, S[32 * half + pp], sc[pp]);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) st_chunk(sW, tid, q, pack8(S + 8 * q));
+        }
+        // ---- (h) y = Yd + exp(Lam_t) Yo + D x (x gate), written over X in place
         {
             const float et = ex2_approx(lam);
 #pragma unroll
@@ -355,17 +362,15 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_tc_kernel(const __grid_consta
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const f2 xf = ptx::bf2_to_f2(xin[e]);
-                        const int j = 8 * q + 2 * e;
-                        float y0 = fmaf(et, yo[j], yd[j]);
-                        float y1 = fmaf(et, yo[j + 1], yd[j + 1]);
-                        y0 = fmaf(Dh, xf.x, y0);
-                        y1 = fmaf(Dh, xf.y, y1);
+                        const int jj = 8 * q + 2 * e;
+                        f2 y = ptx::fma2(f2{et, et}, f2{yo[jj], yo[jj + 1]}, f2{yd[jj], yd[jj + 1]});
+                        y = ptx::fma2(f2{Dh, Dh}, xf, y);
                         if (kGate) {
                             const f2 zf = ptx::bf2_to_f2(zin[e]);
-                            y0 *= silu<true>(zf.x);
-                            y1 *= silu<true>(zf.y);
+                            y.x *= silu<true>(zf.x);
+                            y.y *= silu<true>(zf.y);
                         }
-                        out[e] = ptx::f2_to_bf2(y0, y1);
+                        out[e] = ptx::f2_to_bf2(y.x, y.y);
                     }
                     st_chunk(sX, tid, qq, make_uint4(out[0], out[1], out[2], out[3]));
                 }
@@ -452,14 +457,14 @@ cudaError_t launch_ssd_tc(const SSDParams &p, cudaStream_t stream) {
     cudaError_t e;
     if (p.z) {
         e = cudaFuncSetAttribute(ssd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
+                                 Smem<true>::bytes);
         if (e != cudaSuccess) return e;
-        ssd_tc_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(m, p);
+        ssd_tc_kernel<true><<<grid, kThreads, Smem<true>::bytes, stream>>>(m, p);
     } else {
         e = cudaFuncSetAttribute(ssd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes);
+                                 Smem<false>::bytes);
         if (e != cudaSuccess) return e;
-        ssd_tc_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(m, p);
+        ssd_tc_kernel<false><<<grid, kThreads, Smem<false>::bytes, stream>>>(m, p);
     }
     return cudaGetLastError();
 }
