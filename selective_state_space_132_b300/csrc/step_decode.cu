@@ -19,6 +19,19 @@ namespace {
 
 constexpr int kBlock = 256;
 
+// Four consecutive I/O values (B or C of one lane's states) as floats.
+template <typename TIO> __device__ __forceinline__ void load4(const TIO *p, float (&v)[4]);
+template <> __device__ __forceinline__ void load4<float>(const float *p, float (&v)[4]) {
+    const float4 q = __ldg(reinterpret_cast<const float4 *>(p));
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16 *p, float (&v)[4]) {
+    const uint2 q = __ldg(reinterpret_cast<const uint2 *>(p));
+    v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xffff0000u);
+    v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
+}
+
 template <typename TIO, int LPC, bool kFast, bool kVec>
 __global__ void __launch_bounds__(kBlock) decode_kernel(DecodeParams p) {
     const TIO *__restrict__ gx = static_cast<const TIO *>(p.x);
@@ -40,27 +53,35 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(DecodeParams p) {
     float acc = 0.f, xv = 0.f;
     if (valid) {
         xv = Io<TIO>::load(gx + row);
-        const float bias = p.bias ? p.bias[d] : 0.f;
+        const float bias = p.bias ? __ldg(p.bias + d) : 0.f;
         const float dl = step_size<kFast>(Io<TIO>::load(gdl + row), bias, p.softplus);
         const float dx = dl * xv;
         const int n0 = j * 4;
         float *st = p.state + row * N + n0;
-        float h[4];
+        float h[4], a[4], bv[4], cv[4];
         if (kVec) {
+            // whole rows of four states: 16-byte state and A accesses, 8- or 16-byte B, C
             const float4 s4 = *reinterpret_cast<const float4 *>(st);
             h[0] = s4.x; h[1] = s4.y; h[2] = s4.z; h[3] = s4.w;
+            const float4 a4 = __ldg(reinterpret_cast<const float4 *>(p.A + d * N + n0));
+            a[0] = a4.x; a[1] = a4.y; a[2] = a4.z; a[3] = a4.w;
+            load4<TIO>(gB + b * N + n0, bv);
+            load4<TIO>(gC + b * N + n0, cv);
         } else {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) h[k] = (n0 + k < N) ? st[k] : 0.f;
+            for (int k = 0; k < 4; ++k) {
+                const bool in = n0 + k < N;
+                h[k] = in ? st[k] : 0.f;
+                a[k] = in ? __ldg(p.A + d * N + n0 + k) : 0.f;
+                bv[k] = in ? Io<TIO>::load(gB + b * N + n0 + k) : 0.f;
+                cv[k] = in ? Io<TIO>::load(gC + b * N + n0 + k) : 0.f;
+            }
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int n = n0 + k;
-            if (kVec || n < N) {
-                const float a = decay<kFast>(dl, scale_A<kFast>(p.A[d * N + n]));
-                h[k] = fmaf(a, h[k], dx * Io<TIO>::load(gB + b * N + n));
-                acc = fmaf(Io<TIO>::load(gC + b * N + n), h[k], acc);
-            }
+            const float da = decay<kFast>(dl, scale_A<kFast>(a[k]));
+            h[k] = fmaf(da, h[k], dx * bv[k]);
+            acc = fmaf(cv[k], h[k], acc);
         }
         if (kVec) {
             *reinterpret_cast<float4 *>(st) = make_float4(h[0], h[1], h[2], h[3]);
@@ -73,7 +94,7 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(DecodeParams p) {
 #pragma unroll
     for (int off = LPC / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (valid && j == 0) {
-        float out = acc + (p.Dv ? p.Dv[d] * xv : 0.f);
+        float out = acc + (p.Dv ? __ldg(p.Dv + d) * xv : 0.f);
         if (gz) out *= silu<kFast>(Io<TIO>::load(gz + row));
         gy[row] = Io<TIO>::from_f(out);
     }
@@ -82,8 +103,13 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(DecodeParams p) {
 template <typename TIO, int LPC>
 cudaError_t launch_lpc(const DecodeParams &p, cudaStream_t stream) {
     constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
+    // the vector path needs whole rows of four states and aligned row starts
+    const size_t e = sizeof(TIO);
     const bool vec = (p.dstate == 4 * LPC) &&
-                     (reinterpret_cast<uintptr_t>(p.state) % 16 == 0);
+                     (reinterpret_cast<uintptr_t>(p.state) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(p.A) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(p.Bm) % (4 * e) == 0) &&
+                     (reinterpret_cast<uintptr_t>(p.Cm) % (4 * e) == 0);
     const int64_t threads = p.batch * p.dim * LPC;
     const unsigned grid = static_cast<unsigned>((threads + kBlock - 1) / kBlock);
     if (vec)
