@@ -49,7 +49,7 @@ WORKLOADS = {
     "ssd_bf16_B4_L8192_H80_P64_N128_G1_Q256": 3,
     "decode_bf16_B256_D5120_N16_x1000": 4,
 }
-SCAN_SOURCES = ["scan_fwd.cu", "common.cuh"]
+SCAN_SOURCES = ["scan_tma.cu", "scan_fwd.cu", "common.cuh", "ptx.cuh", "internal.h"]
 
 
 # ------------------------------------------------------------------ small helpers
@@ -355,6 +355,41 @@ def time_decode(p, steps, flush, device, pool=8):
     return float(np.median(flushed)), a.elapsed_time(b) * 1e-3 / steps
 
 
+def ssd_decode_bytes_per_step(nb, H, P, G, N, e):
+    return 2 * nb * H * P * N * 4 + 2 * nb * H * P * e + nb * H * e + 2 * nb * G * N * e + 3 * H * 4
+
+
+def time_ssd_decode(nb, H, P, G, N, flush, device, iters=30):
+    """Median per-step time of ssm_ssd_step_decode (multi-head decode step, state in
+    place) with L2 flushed before each step; seeded synthetic state and tokens."""
+    import torch
+    import selective_state_space_132_b300 as ssm
+    p = W.ssd_problem(nb, 1, H, P, G, N, io="bf16", seed=1005, h0=True)
+    t = _to_dev(device)
+    io = torch.bfloat16
+    state = t(p.h0)
+    x, dl = t(p.x[:, 0], io), t(p.delta[:, 0], io)
+    Bm, Cm = t(p.B[:, 0], io), t(p.C[:, 0], io)
+    A, Dv, bias = t(p.A), t(p.D), t(p.bias)
+    y = torch.empty_like(x)
+
+    def step():
+        ssm.ssd_step_decode(state, x, dl, A, Bm, Cm, D=Dv, delta_bias=bias, y=y)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e-3)
+    return float(np.median(times))
+
+
 def cpu_baseline_scan(p, target_s=10.0, max_s=30.0):
     """The fp64 oracle as it stands, all host cores, on a bounded channel sample of
     the workload; returns updates/s and what the sample was."""
@@ -457,11 +492,12 @@ def extras(device, flush, hbm, tf_sus):
     p = W.config_problem(3)
     s = time_ssd(p, 5, flush, device)
     b = ssd_bytes(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, 2)
-    fl = ssd_flops(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, p.chunk)
+    # the tensor-core kernel works in 128-step chunks whatever chunk_size asks for
+    fl = ssd_flops(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, 128)
     res["ssd_bf16_B4_L8192_H80_P64_N128_G1_Q256"] = {
         "ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
         "hbm_frac": b / s / 1e9 / hbm, "tensor_tflops": fl / s / 1e12,
-        "tensor_frac_sustained": fl / s / 1e12 / tf_sus}
+        "tensor_frac_sustained": fl / s / 1e12 / tf_sus, "kernel_chunk": 128}
     del p
     torch.cuda.empty_cache()
     p = W.config_problem(4)
@@ -473,6 +509,13 @@ def extras(device, flush, hbm, tf_sus):
         "hbm_frac_l2_flushed": b / s_flush / 1e9 / hbm,
         "gbs_back_to_back": b / s_hot / 1e9,
         "note": "back-to-back steps keep much of the 84 MB state in the 126 MB L2"}
+    del p
+    torch.cuda.empty_cache()
+    s = time_ssd_decode(64, 80, 64, 1, 128, flush, device)
+    b = ssd_decode_bytes_per_step(64, 80, 64, 1, 128, 2)
+    res["ssd_decode_bf16_B64_H80_P64_N128"] = {
+        "ms_per_step_l2_flushed": s * 1e3, "updates_per_s": 64 * 80 * 64 * 128 / s,
+        "gbs_l2_flushed": b / s / 1e9, "hbm_frac_l2_flushed": b / s / 1e9 / hbm}
     return res
 
 

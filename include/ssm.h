@@ -182,6 +182,29 @@ typedef struct {
 
 SSM_API ssm_status ssm_step_decode(const ssm_decode_args *args, ssm_stream_t stream);
 
+/* ------------------------------------------------------------------ multi-head decode step
+ * One token of the multi-head scalar-A recurrence that ssm_ssd_chunk_fwd computes in
+ * its chunked form ("Mamba-2: 상태 공간 기반 시퀀스 모델", section "멀티-헤드 구조";
+ * tildalice review, section "추론 속도" for the fixed-size state).  Per sequence b and
+ * head h (group g = h / (H / G)), dl = softplus(delta + bias_h):
+ *   S[p, :] <- exp(dl A_h) S[p, :] + dl x_p B_g ;   y_p = S[p, :] . C_g + D_h x_p  (x silu(z_p))
+ * Shapes: state (B, H, P, N) fp32, read and written IN PLACE;
+ *   x, z, y : (B, H, P) io_dtype     delta : (B, H) io_dtype
+ *   B, C    : (B, G, N) io_dtype     A, D, delta_bias : (H) fp32
+ * Nullable: D, delta_bias, z.  H % G == 0, 1 <= N <= 256.  L calls on one stream equal
+ * one ssm_ssd_chunk_fwd over the same L tokens (up to rounding).  No workspace. */
+typedef struct {
+    int64_t batch, nheads, headdim, ngroups, dstate;
+    int32_t io_dtype;
+    int32_t delta_softplus;
+    float *state;
+    const void *x, *delta, *B, *C, *z;
+    const float *A, *D, *delta_bias;
+    void *y;
+} ssm_ssd_decode_args;
+
+SSM_API ssm_status ssm_ssd_step_decode(const ssm_ssd_decode_args *args, ssm_stream_t stream);
+
 /* ------------------------------------------------------------------ utilities */
 SSM_API const char *ssm_status_string(ssm_status status);
 SSM_API int ssm_version(void); /* major * 10000 + minor * 100 + patch */
@@ -190,6 +213,17 @@ SSM_API int ssm_version(void); /* major * 10000 + minor * 100 + patch */
  * the last call using `workspace` left there (SSM_OK when none failed). */
 SSM_API ssm_status ssm_read_device_status(const void *workspace, ssm_stream_t stream,
                                   ssm_status *device_status);
+
+/* Diagnostic, no counterpart in the pages.  Every spin-wait in the kernels is bounded;
+ * this call shows what happens when one runs out.  It clears the 256-byte status header
+ * at `workspace` (256-byte aligned), then runs one thread that waits, through the same
+ * acquire-and-back-off routine the SSD kernel uses to take over the state of the block
+ * before it, on a flag that nothing sets.  After `budget_cycles` SM clock cycles
+ * (1 .. 2e9; about 1 ms per 2e6 on B300) the wait gives up and the kernel records
+ * SSM_ERR_TIMEOUT, which ssm_read_device_status then returns; the CUDA context stays
+ * usable.  Asynchronous on `stream`. */
+SSM_API ssm_status ssm_check_bounded_wait(void *workspace, int64_t budget_cycles,
+                                          ssm_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -55,6 +55,8 @@ def _load():
     lib.oracle_decode_f64.restype = ctypes.c_int
     lib.oracle_decode_f64.argtypes = [i64, i64, i64, dp] + [dp] * 8 + [ctypes.c_int, dp,
                                                                     ctypes.c_int]
+    lib.oracle_ssd_decode_f64.restype = ctypes.c_int
+    lib.oracle_ssd_decode_f64.argtypes = [i64] * 5 + [dp] * 9 + [ctypes.c_int, dp, ctypes.c_int]
     lib.oracle_softplus_f64.restype = ctypes.c_double
     lib.oracle_softplus_f64.argtypes = [ctypes.c_double]
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -144,6 +146,30 @@ def decode_step(state, x, delta, A, Bm, Cm, Dv=None, z=None, bias=None,
                                _ptr(y), threads or default_threads())
     if rc != 0:
         raise RuntimeError(f"oracle_decode_f64 failed: {rc}")
+    return y
+
+
+def ssd_decode_step(state, x, delta, A, Bm, Cm, Dv=None, z=None, bias=None,
+                    softplus: bool = True, threads: Optional[int] = None):
+    """One token of the multi-head scalar-A recurrence.  state: (B,H,P,N) float64,
+    UPDATED IN PLACE; x, z: (B,H,P); delta: (B,H); Bm, Cm: (B,G,N); A, Dv, bias: (H,).
+    Returns y (B,H,P)."""
+    lib = _load()
+    if not (isinstance(state, np.ndarray) and state.dtype == np.float64
+            and state.flags.c_contiguous):
+        raise TypeError("state must be a C-contiguous float64 numpy array")
+    x, delta, A, Bm, Cm = map(_f64, (x, delta, A, Bm, Cm))
+    Dv, z, bias = map(_f64, (Dv, z, bias))
+    nb, H, P, N = state.shape
+    G = Bm.shape[1]
+    assert x.shape == (nb, H, P) and delta.shape == (nb, H) and A.shape == (H,)
+    assert Bm.shape == (nb, G, N) and Cm.shape == Bm.shape and H % G == 0
+    y = np.empty((nb, H, P), np.float64)
+    rc = lib.oracle_ssd_decode_f64(nb, H, P, G, N, _ptr(state), _ptr(x), _ptr(delta), _ptr(A),
+                                   _ptr(Bm), _ptr(Cm), _ptr(Dv), _ptr(z), _ptr(bias),
+                                   int(bool(softplus)), _ptr(y), threads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_ssd_decode_f64 failed: {rc}")
     return y
 
 

@@ -171,6 +171,43 @@ int oracle_decode_f64(int64_t nb, int64_t D, int64_t N, double *state,
     return 0;
 }
 
+/* One token of the multi-head scalar-A recurrence (the SSD form's decode step): per
+ * batch b and head hd (group g = hd / (H / G)), with dl = step(delta[b,hd]):
+ *   S[p,n] <- exp(dl A[hd]) S[p,n] + dl x[b,hd,p] B[b,g,n]   (state updated in place)
+ *   y[b,hd,p] = sum_n C[b,g,n] S[p,n] + D[hd] x[b,hd,p], times silu(z) if given.
+ * Layouts: state (B,H,P,N); x, z, y (B,H,P); delta (B,H); Bm, Cm (B,G,N); A, Dv, bias (H). */
+int oracle_ssd_decode_f64(int64_t nb, int64_t H, int64_t P, int64_t G, int64_t N, double *state,
+                          const double *x, const double *delta, const double *A,
+                          const double *Bm, const double *Cm, const double *Dv,
+                          const double *z, const double *bias, int softplus, double *y,
+                          int nthreads)
+{
+    if (nb < 0 || H < 1 || P < 1 || G < 1 || N < 1 || H % G) return -1;
+    if (nthreads < 1) nthreads = 1;
+    int64_t heads_per_group = H / G;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int64_t c = 0; c < nb * H; ++c) {
+        int64_t b = c / H, hd = c % H, g = hd / heads_per_group;
+        double dl = step_size(delta[c], bias, hd, softplus);
+        double decay = exp(dl * A[hd]);
+        const double *Bt = Bm + (b * G + g) * N;
+        const double *Ct = Cm + (b * G + g) * N;
+        for (int64_t p = 0; p < P; ++p) {
+            double xv = x[c * P + p];
+            double *Sp = state + (c * P + p) * N;
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                Sp[n] = decay * Sp[n] + dl * xv * Bt[n];
+                acc += Ct[n] * Sp[n];
+            }
+            double out = acc + (Dv ? Dv[hd] : 0.0) * xv;
+            if (z) out *= silu_f64(z[c * P + p]);
+            y[c * P + p] = out;
+        }
+    }
+    return 0;
+}
+
 /* Helper exposed for the pins: the scalar softplus used above. */
 double oracle_softplus_f64(double v) { return softplus_f64(v); }
 

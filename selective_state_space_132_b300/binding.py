@@ -18,7 +18,7 @@ _STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED",
 
 EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
             "ssm_ssd_workspace_size", "ssm_ssd_chunk_fwd", "ssm_ssd_plan", "ssm_step_decode",
-            "ssm_status_string", "ssm_version",
+            "ssm_ssd_step_decode", "ssm_status_string", "ssm_version", "ssm_check_bounded_wait",
             "ssm_read_device_status"]
 
 _i64, _i32, _vp, _fp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p
@@ -47,6 +47,13 @@ class DecodeArgs(ctypes.Structure):
     _fields_ = [("batch", _i64), ("dim", _i64), ("dstate", _i64),
                 ("io_dtype", _i32), ("delta_softplus", _i32), ("state", _fp),
                 ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp), ("z", _vp),
+                ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("y", _vp)]
+
+
+class SSDDecodeArgs(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("nheads", _i64), ("headdim", _i64), ("ngroups", _i64),
+                ("dstate", _i64), ("io_dtype", _i32), ("delta_softplus", _i32),
+                ("state", _fp), ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp), ("z", _vp),
                 ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("y", _vp)]
 
 
@@ -90,7 +97,11 @@ def load_library():
     lib.ssm_ssd_chunk_fwd.argtypes = [ctypes.POINTER(SSDArgs), _vp]
     lib.ssm_ssd_plan.argtypes = [ctypes.POINTER(SSDArgs), ctypes.POINTER(ctypes.c_int32)]
     lib.ssm_step_decode.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+    lib.ssm_ssd_step_decode.argtypes = [ctypes.POINTER(SSDDecodeArgs), _vp]
+    lib.ssm_ssd_step_decode.restype = ctypes.c_int
     lib.ssm_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
+    lib.ssm_check_bounded_wait.argtypes = [_vp, ctypes.c_int64, _vp]
+    lib.ssm_check_bounded_wait.restype = ctypes.c_int
     for fn in ("ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
                "ssm_ssd_workspace_size", "ssm_ssd_chunk_fwd", "ssm_ssd_plan", "ssm_step_decode",
                "ssm_read_device_status"):
@@ -357,4 +368,37 @@ def step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: to
                       _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
                       _ptr(delta_bias), _ptr(y))
     _raise(lib.ssm_step_decode(ctypes.byref(args), _stream(stream)), "ssm_step_decode")
+    return y
+
+
+# ---------------------------------------------------------------- multi-head decode
+def ssd_step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor,
+                    B: torch.Tensor, C: torch.Tensor, D: Optional[torch.Tensor] = None,
+                    z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
+                    delta_softplus: bool = True, y: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """One token of the multi-head scalar-A recurrence; ``state`` (B, H, P, N) fp32 is
+    updated in place.  x, z: (B, H, P); delta: (B, H); B, C: (B, G, N); A, D,
+    delta_bias: (H,) fp32."""
+    lib = load_library()
+    nb, H, P, N = state.shape
+    G = B.shape[1]
+    dev, io = x.device, x.dtype
+    _io_code(x)
+    _check(state, "state", (nb, H, P, N), torch.float32, dev)
+    _check(x, "x", (nb, H, P), io, dev)
+    _check(delta, "delta", (nb, H), io, dev)
+    _check(A, "A", (H,), torch.float32, dev)
+    _check(B, "B", (nb, G, N), io, dev)
+    _check(C, "C", (nb, G, N), io, dev)
+    _check(D, "D", (H,), torch.float32, dev)
+    _check(z, "z", (nb, H, P), io, dev)
+    _check(delta_bias, "delta_bias", (H,), torch.float32, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    _check(y, "y", (nb, H, P), io, dev)
+    args = SSDDecodeArgs(nb, H, P, G, N, _io_code(x), int(bool(delta_softplus)), _ptr(state),
+                         _ptr(x), _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
+                         _ptr(delta_bias), _ptr(y))
+    _raise(lib.ssm_ssd_step_decode(ctypes.byref(args), _stream(stream)), "ssm_ssd_step_decode")
     return y

@@ -24,25 +24,18 @@ struct ScanParams {
     int clear_status;   // the first block of this launch clears the status word
 };
 
-// Lanes per channel of the TMA scan at N = 16 (2: 8 states per lane, 16
-// channels per block; 4: 4 states per lane, 8 channels per block).
-#ifndef SSM_SCAN_LANES16
-#define SSM_SCAN_LANES16 4
-#endif
-constexpr int kScanLanes16 = SSM_SCAN_LANES16;
-
-// TMA-staged scan (scan_tma.cu): lanes per channel for N (0 = not supported),
-// whether a call can take it, and the launch.
-int scan_tma_lanes(int64_t dstate);
+// TMA-staged scan (scan_tma.cu): warps per 32-channel block for these sizes (0 = the
+// sizes are not supported), whether a call can take it, and the launch.
+int scan_tma_block_warps(int io_bf16, int64_t dstate);
 bool scan_tma_sizes_ok(int io_bf16, int64_t seqlen, int64_t dim, int64_t dstate);
 bool scan_tma_pointers_ok(const void *const *ptrs, int nptrs);
 int device_sm_count();
 cudaError_t launch_scan_tma(const ScanParams &p, cudaStream_t stream);
 
-// Number of time chunks and chunk length the scan uses for these sizes; `tma`
-// selects the plan of the TMA-staged path (its blocks hold 32 / lanes channels).
+// Number of time chunks and chunk length the scan uses for these sizes; `tma_warps` > 0
+// selects the plan of the TMA-staged path (blocks of 32 channels and that many warps).
 void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t time_chunk,
-               bool tma, int64_t *chunk_len, int *nchunks);
+               int tma_warps, int64_t *chunk_len, int *nchunks);
 size_t scan_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, int nchunks);
 cudaError_t launch_scan(const ScanParams &p, cudaStream_t stream);
 
@@ -70,10 +63,23 @@ struct SSDParams {
     size_t work_bytes;
 };
 size_t ssd_workspace_bytes(const SSDParams &p);
+// Bytes at the start of the workspace the call must zero (status word, hand-over flags).
+size_t ssd_clear_bytes(const SSDParams &p);
 cudaError_t launch_ssd(const SSDParams &p, cudaStream_t stream);
 cudaError_t launch_ssd_recurrent(const SSDParams &p, cudaStream_t stream);
 // Chunked dual form on tcgen05 (ssd_tc.cu): bf16 I/O, headdim 64, dstate 128.
 bool ssd_tc_eligible(const SSDParams &p);
 cudaError_t launch_ssd_tc(const SSDParams &p, cudaStream_t stream);
+
+struct SSDDecodeParams {
+    int64_t batch, nheads, headdim, ngroups, dstate;
+    int io_bf16;
+    int softplus;
+    float *state;
+    const void *x, *delta, *Bm, *Cm, *z;
+    const float *A, *Dv, *bias;
+    void *y;
+};
+cudaError_t launch_ssd_decode(const SSDDecodeParams &p, cudaStream_t stream);
 
 }  // namespace ssm

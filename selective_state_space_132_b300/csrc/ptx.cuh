@@ -83,6 +83,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *tm, const void *
         "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// L2 prefetch of a 3-D tile (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *tm, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -92,6 +99,26 @@ template <int N> __device__ __forceinline__ void bulk_wait_read() {
 }
 template <int N> __device__ __forceinline__ void bulk_wait() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------- release / acquire flags
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Spin (with back-off) until *flag != 0, acquiring what its writer released; false if
+// `budget` clock cycles pass first.
+__device__ __forceinline__ bool wait_flag(const uint32_t *flag, long long budget) {
+    const long long t0 = clock64();
+    while (ld_acquire_u32(flag) == 0u) {
+        if (clock64() - t0 > budget) return false;
+        __nanosleep(256);
+    }
+    return true;
 }
 
 // ---------------------------------------------------------------- packed fp32x2

@@ -39,6 +39,7 @@ namespace ssm {
 namespace {
 
 constexpr int kTT = 32;  // time steps per shared-memory tile
+constexpr int kTmaWarpsPerSm = 8;
 constexpr int kDT = 32;  // channels per thread block
 constexpr int kRowF = kTT + 4;  // floats per per-channel row (16-byte aligned, conflict-free)
 
@@ -351,20 +352,18 @@ int device_sm_count() {
 }
 
 void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t time_chunk,
-               bool tma, int64_t *chunk_len, int *nchunks) {
+               int tma_warps, int64_t *chunk_len, int *nchunks) {
     int64_t cl;
     if (time_chunk > 0) {
         cl = (time_chunk + kTT - 1) / kTT * kTT;
     } else {
-        // Enough warps to fill every SM about eight (general kernel) or ten (TMA
-        // kernel, one warp per block) deep.  Each extra chunk costs a summary pass
-        // over that chunk (most of a scan of it), so split only when short of it and
-        // keep chunks at least 1024 steps long.
+        // Enough warps to keep every SM busy, about eight deep.  Each extra chunk costs a
+        // summary pass over that chunk (most of a scan of it), so split only when short
+        // of it and keep chunks at least 1024 steps long.
         int64_t warps, target;
-        if (tma) {
-            // blocks of 32 channels with one warp per lane slot of a channel
-            warps = batch * ((dim + 31) / 32) * scan_tma_lanes(dstate);
-            target = static_cast<int64_t>(device_sm_count()) * 10;
+        if (tma_warps > 0) {
+            warps = batch * ((dim + 31) / 32) * tma_warps;
+            target = static_cast<int64_t>(device_sm_count()) * kTmaWarpsPerSm;
         } else {
             warps = batch * ((dim + kDT - 1) / kDT) * lanes_for(dstate);
             target = static_cast<int64_t>(device_sm_count()) * 8;

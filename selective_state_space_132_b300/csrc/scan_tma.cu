@@ -524,22 +524,24 @@ cudaError_t launch_tma_pair(ScanParams p, cudaStream_t stream) {
 
 }  // namespace
 
-int scan_tma_lanes(int64_t dstate) {
+// Lane slots per channel (LPC, NS = N / LPC states per lane) for each supported N;
+// 32-channel blocks hold LPC warps of 32 / LPC channels.
+static int scan_tma_lpc(int io_bf16, int64_t dstate) {
     switch (dstate) {
-        case 4: return 2;
+        case 4: return io_bf16 ? 0 : 2;  // 8-byte bf16 B/C rows are below the TMA minimum
         case 8: return 2;
-        case 16: return kScanLanes16;
+        case 16: return 4;
         case 32: return 4;
         case 64: return 4;
         default: return 0;
     }
 }
 
+int scan_tma_block_warps(int io_bf16, int64_t dstate) { return scan_tma_lpc(io_bf16, dstate); }
+
 bool scan_tma_sizes_ok(int io_bf16, int64_t seqlen, int64_t dim, int64_t dstate) {
     const int64_t e = io_bf16 ? 2 : 4;
-    const int lpc = scan_tma_lanes(dstate);
-    if (lpc == 0) return false;
-    if (io_bf16 && dstate == 4) return false;  // 8-byte B/C rows are below the TMA minimum
+    if (scan_tma_lpc(io_bf16, dstate) == 0) return false;
     if (dstate * e % 16 != 0 || dim * e % 16 != 0) return false;
     return seqlen > 0 && seqlen < (int64_t(1) << 31) && dim < (int64_t(1) << 31);
 }
@@ -555,14 +557,14 @@ cudaError_t launch_scan_tma(const ScanParams &p, cudaStream_t stream) {
     if (p.io_bf16) {
         using T = __nv_bfloat16;
         if (N == 8) return launch_tma_pair<T, 4, 2>(p, stream);
-        if (N == 16) return launch_tma_pair<T, 16 / kScanLanes16, kScanLanes16>(p, stream);
+        if (N == 16) return launch_tma_pair<T, 4, 4>(p, stream);
         if (N == 32) return launch_tma_pair<T, 8, 4>(p, stream);
         if (N == 64) return launch_tma_pair<T, 16, 4>(p, stream);
     } else {
         using T = float;
         if (N == 4) return launch_tma_pair<T, 2, 2>(p, stream);
         if (N == 8) return launch_tma_pair<T, 4, 2>(p, stream);
-        if (N == 16) return launch_tma_pair<T, 16 / kScanLanes16, kScanLanes16>(p, stream);
+        if (N == 16) return launch_tma_pair<T, 4, 4>(p, stream);
         if (N == 32) return launch_tma_pair<T, 8, 4>(p, stream);
         if (N == 64) return launch_tma_pair<T, 16, 4>(p, stream);
     }

@@ -111,7 +111,6 @@ cudaError_t launch_ssd_recurrent(const SSDParams &p, cudaStream_t stream) {
                      : launch_rec_typed<float>(p, stream);
 }
 
-size_t ssd_workspace_bytes(const SSDParams &) { return kStatusBytes; }
 
 cudaError_t launch_ssd(const SSDParams &p, cudaStream_t stream) {
     if (ssd_tc_eligible(p)) return launch_ssd_tc(p, stream);

@@ -41,6 +41,8 @@
 // sequential kernel (ssd_chunk.cu).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "../../include/ssm.h"
 #include "common.cuh"
 #include "internal.h"
@@ -94,9 +96,25 @@ __device__ __forceinline__ uint4 pack8(const float *v) {
                       ptx::f2_to_bf2(v[4], v[5]), ptx::f2_to_bf2(v[6], v[7]));
 }
 
+// Work split over a persistent grid (stream-K): the B * H chains of nch chunks each
+// form units = B * H * nch chunk steps; block k takes steps [u0, u1).  A chain cut
+// between blocks k and k + 1 hands its state over through the workspace: block k
+// runs that chain's head first and publishes the state (flag[k] = 1, release);
+// block k + 1 runs its other work first and that chain's tail last, after
+// acquiring the flag.  With at least one chain per block a chain is cut at most
+// once and, since head + tail = nch <= the steps of a block, no block waits in
+// steady state.
+struct Split {
+    int nctas;
+    int nch;           // chunks per chain
+    int64_t units;
+    uint32_t *flags;   // nctas flags, zeroed before the launch
+    float *states;     // nctas states of P x N fp32
+};
+
 template <bool kGate>
 __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_constant__ Maps maps,
-                                                             SSDParams p) {
+                                                             SSDParams p, Split sk) {
     using SM = Smem<kGate>;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *sC = smem + o_C, *sB = smem + o_B, *sX = smem + o_X, *sW = smem + o_W;
@@ -111,9 +129,8 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x, b = blockIdx.y;
+    const int k = blockIdx.x;
     const int64_t H = p.nheads, L = p.seqlen;
-    const int g = static_cast<int>(h / (H / p.ngroups));
     const __nv_bfloat16 *gdt = static_cast<const __nv_bfloat16 *>(p.delta);
     DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
 
@@ -122,10 +139,6 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         if (tid == 0) report_status(status, SSM_ERR_UNSUPPORTED, 29);
         return;
     }
-
-    const float a_l2 = p.A[h] * kLog2e;  // decay exponent per unit step, base 2
-    const float bias = p.bias ? p.bias[h] : 0.f;
-    const float Dh = p.Dv ? p.Dv[h] : 0.f;
 
     if (tid == 0) {
         ptx::mbar_init(bar_load, 1);
@@ -142,17 +155,6 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
     const uint32_t tmem = *s_tmem;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
 
-    // fp32 state, row n = tid of S^T: S[p][n] for p = 0..63; bf16 copy in sW
-    float S[kP];
-    {
-        const float *h0 = p.h0 ? p.h0 + (static_cast<int64_t>(b) * H + h) * kP * kN : nullptr;
-#pragma unroll
-        for (int pp = 0; pp < kP; ++pp) S[pp] = h0 ? h0[pp * kN + tid] : 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) st_chunk(sW, tid, q, pack8(S + 8 * q));
-    }
-    ptx::fence_proxy_async_smem();  // the first Yo MMA reads sW
-
     const uint32_t id_G = ptx::idesc_bf16(128, 128, 0, 0);
     const uint32_t id_Yo = ptx::idesc_bf16(128, kP, 0, 1);
     const uint32_t id_Sc = ptx::idesc_bf16(128, kP, 1, 1);
@@ -163,225 +165,310 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
 
     uint32_t ph_load = 0, ph_mma = 0;
     bool ok = true;
-    int pending = 0;  // 1: a TMA load, 2: an MMA commit that did not arrive in time
+    int pending = 0;  // 1: a TMA load, 2: an MMA commit, 3: a state hand-over that timed out
     // Every thread waits; the block agrees on the outcome so that it never splits.
     auto wait_all = [&](uint64_t *bar, uint32_t ph) -> bool {
         const int mine = ptx::mbar_wait(bar, ph) ? 1 : 0;
         return __syncthreads_and(mine) != 0;
     };
-    const int nchunks = static_cast<int>((L + kQ - 1) / kQ);
 
-    for (int c = 0; c < nchunks; ++c) {
-        const int t0 = c * kQ;
-        // ---- (a) loads of this chunk (the previous chunk released every tile)
-        if (tid == 0) {
-            ptx::bulk_wait_read<0>();  // y store of the previous chunk has left sX
-            ptx::mbar_arrive_expect_tx(bar_load, kLoadBytes);
-            for (int kb = 0; kb < 2; ++kb) {
-                ptx::tma_load_3d(sC + kb * kTile, &maps.C, bar_load, g * kN + 64 * kb, t0, b);
-                ptx::tma_load_3d(sB + kb * kTile, &maps.B, bar_load, g * kN + 64 * kb, t0, b);
+    // ---- this block's steps: head of the last chain, whole chains, tail of the first
+    const int nch = sk.nch;
+    const int64_t u0 = static_cast<int64_t>(k) * sk.units / sk.nctas;
+    const int64_t u1 = static_cast<int64_t>(k + 1) * sk.units / sk.nctas;
+    const int64_t first = u0 / nch, last = (u1 - 1) / nch;
+    const int first_off = static_cast<int>(u0 - first * nch);
+    const int last_end = static_cast<int>(u1 - last * nch);
+    const bool has_tail = u1 > u0 && first_off > 0;
+    const bool has_head = u1 > u0 && last_end < nch && !(has_tail && first == last);
+    const int64_t full_lo = has_tail ? first + 1 : first;
+    const int64_t full_hi = has_head ? last : last + 1;  // exclusive
+    const int64_t nfull = full_hi > full_lo ? full_hi - full_lo : 0;
+    const int nseg = (u1 > u0) ? (has_head ? 1 : 0) + static_cast<int>(nfull) + (has_tail ? 1 : 0)
+                               : 0;
+
+    float S[kP];
+    for (int seg = 0; seg < nseg && ok; ++seg) {
+        // kind: 1 head (publishes), 0 whole chain, 2 tail (acquires)
+        int kind;
+        int64_t chain;
+        int c_lo, c_hi;
+        if (has_head && seg == 0) {
+            kind = 1; chain = last; c_lo = 0; c_hi = last_end;
+        } else if (has_tail && seg == nseg - 1) {
+            kind = 2; chain = first; c_lo = first_off; c_hi = nch;
+        } else {
+            kind = 0; chain = full_lo + (seg - (has_head ? 1 : 0)); c_lo = 0; c_hi = nch;
+        }
+        const int b = static_cast<int>(chain / H), h = static_cast<int>(chain % H);
+        const int g = static_cast<int>(h / (H / p.ngroups));
+        const float a_l2 = p.A[h] * kLog2e;  // decay exponent per unit step, base 2
+        const float bias = p.bias ? p.bias[h] : 0.f;
+        const float Dh = p.Dv ? p.Dv[h] : 0.f;
+
+        // ---- initial state: h0 (or zero), or the state the previous block handed over
+        const float *src;
+        if (kind == 2) {
+            int got = 1;
+            if (tid == 0) got = ptx::wait_flag(sk.flags + (k - 1), ptx::kWaitCycles) ? 1 : 0;
+            if (__syncthreads_or(tid == 0 && !got)) {
+                ok = false;
+                pending = 3;
+                break;
             }
-            ptx::tma_load_3d(sX, &maps.X, bar_load, h * kP, t0, b);
-            if (kGate) ptx::tma_load_3d(sZ, &maps.Z, bar_load, h * kP, t0, b);
+            src = sk.states + static_cast<int64_t>(k - 1) * kP * kN;
+        } else {
+            src = p.h0 ? p.h0 + (static_cast<int64_t>(b) * H + h) * kP * kN : nullptr;
         }
-        // ---- (b) step sizes, the running log2-decay and the column factors
-        const int64_t t = t0 + tid;
-        float dl = 0.f;
-        if (t < L) {
-            const float raw = __bfloat162float(gdt[(static_cast<int64_t>(b) * L + t) * H + h]);
-            dl = step_size<true>(raw, bias, p.softplus);
-        }
-        float lam = dl * a_l2;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float v = __shfl_up_sync(0xffffffffu, lam, off);
-            if (lane >= off) lam += v;
-        }
-        // lam of the last step of this warp's 32-step block (before adding earlier warps)
-        const float lam_blk = __shfl_sync(0xffffffffu, lam, 31);
-        if (lane == 31) s_red[warp] = lam;
-        __syncthreads();
-        float base = 0.f;
-        for (int w = 0; w < warp; ++w) base += s_red[w];
-        lam += base;
-        // v_s = exp(Lam_e - Lam_s) dl_s with e the last step of the block holding s
-        s_v[tid] = ex2_approx((base + lam_blk) - lam) * dl;
-        s_dl[tid] = dl;
-        s_lam[tid] = lam;
-
-        if (!wait_all(bar_load, ph_load)) {
-            ok = false;
-            pending = 1;
-            break;
-        }
-        ph_load ^= 1;
-        const float lam_tot = s_red[0] + s_red[1] + s_red[2] + s_red[3];
-
-        // ---- (c) G = C B^T and Yo = C S_in^T
-        if (tid == 0) {
-            ptx::tc_fence_after();
+        for (int pp = 0; pp < kP; ++pp) S[pp] = src ? __ldcg(src + pp * kN + tid) : 0.f;
 #pragma unroll
-            for (int k = 0; k < kN / 16; ++k) {
-                const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
-                const uint64_t da = ptx::sdesc_sw128(aC + off, 16, 1024);
-                const uint64_t db = ptx::sdesc_sw128(aB + off, 16, 1024);
-                ptx::mma_bf16(tmem + kColG, da, db, id_G, k > 0);
-            }
-#pragma unroll
-            for (int k = 0; k < kN / 16; ++k) {
-                const uint32_t off = (k >> 2) * kTile + (k & 3) * 32;
-                const uint64_t da = ptx::sdesc_sw128(aC + off, 16, 1024);
-                const uint64_t db = ptx::sdesc_sw128(aW + k * 2048, 1024, 1024);
-                ptx::mma_bf16(tmem + kColYo, da, db, id_Yo, k > 0);
-            }
-            ptx::mma_commit(bar_mma);
-        }
-        if (!wait_all(bar_mma, ph_mma)) {
-            ok = false;
-            pending = 2;
-            break;
-        }
-        ph_mma ^= 1;
-        ptx::tc_fence_after();
+        for (int q = 0; q < 8; ++q) st_chunk(sW, tid, q, pack8(S + 8 * q));
+        ptx::fence_proxy_async_smem();  // the first Yo MMA reads sW
 
-        // ---- (d) Xw[s, :] = exp(Lam_end - Lam_s) dl_s x_s into sW (S_in is consumed)
+        float raw_next = 0.f;
         {
-            const float w = ex2_approx(lam_tot - lam) * dl;
-            const f2 w2{w, w};
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint4 v = ld_chunk(sX, tid, q);
-                const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-                uint32_t out[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const f2 e = ptx::mul2(ptx::bf2_to_f2(in[i]), w2);
-                    out[i] = ptx::f2_to_bf2(e.x, e.y);
-                }
-                st_chunk(sW, tid, q, make_uint4(out[0], out[1], out[2], out[3]));
-            }
+            const int64_t t = static_cast<int64_t>(c_lo) * kQ + tid;
+            if (t < L) raw_next = __bfloat162float(gdt[(static_cast<int64_t>(b) * L + t) * H + h]);
         }
-        // ---- (e) M[t, s] = G[t, s] exp(Lam_t - Lam_s) dl_s, s <= t, as bf16 pairs over
-        //      G's first 64 columns (row t = tid).  Blocks of 32 columns: below the
-        //      diagonal block exp(Lam_t - Lam_s) = u_t v_s / dl_s with
-        //      u_t = exp(Lam_t - Lam_e), both factors <= 1; on it, pairwise exponentials.
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t packed[16];
-            if (i < warp) {
-                float gv[32];
-                ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
-                const float u = ex2_approx(lam - s_lam[32 * i + 31]);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float2 vv = *reinterpret_cast<const float2 *>(s_v + 32 * i + 2 * e);
-                    const f2 m = ptx::mul2(ptx::mul2(f2{gv[2 * e], gv[2 * e + 1]}, f2{u, u}),
-                                           f2{vv.x, vv.y});
-                    packed[e] = ptx::f2_to_bf2(m.x, m.y);
+
+        for (int c = c_lo; c < c_hi; ++c) {
+            const int t0 = c * kQ;
+            // ---- (a) loads of this chunk (the previous chunk released every tile) and an
+            //      L2 prefetch of the next one
+            if (tid == 0) {
+                ptx::bulk_wait_read<0>();  // y store of the previous chunk has left sX
+                ptx::mbar_arrive_expect_tx(bar_load, kLoadBytes);
+                for (int kb = 0; kb < 2; ++kb) {
+                    ptx::tma_load_3d(sC + kb * kTile, &maps.C, bar_load, g * kN + 64 * kb, t0, b);
+                    ptx::tma_load_3d(sB + kb * kTile, &maps.B, bar_load, g * kN + 64 * kb, t0, b);
                 }
-            } else if (i == warp) {
-                float gv[32];
-                ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float m2[2];
-#pragma unroll
-                    for (int u2 = 0; u2 < 2; ++u2) {
-                        const int s = 32 * i + 2 * e + u2;
-                        const float val = gv[2 * e + u2] * ex2_approx(lam - s_lam[s]) * s_dl[s];
-                        m2[u2] = s <= tid ? val : 0.f;
+                ptx::tma_load_3d(sX, &maps.X, bar_load, h * kP, t0, b);
+                if (kGate) ptx::tma_load_3d(sZ, &maps.Z, bar_load, h * kP, t0, b);
+                if (c + 1 < c_hi) {
+                    for (int kb = 0; kb < 2; ++kb) {
+                        ptx::tma_prefetch_3d(&maps.C, g * kN + 64 * kb, t0 + kQ, b);
+                        ptx::tma_prefetch_3d(&maps.B, g * kN + 64 * kb, t0 + kQ, b);
                     }
-                    packed[e] = ptx::f2_to_bf2(m2[0], m2[1]);
+                    ptx::tma_prefetch_3d(&maps.X, h * kP, t0 + kQ, b);
+                    if (kGate) ptx::tma_prefetch_3d(&maps.Z, h * kP, t0 + kQ, b);
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) packed[e] = 0u;
             }
-            ptx::tmem_st16(tmem + lane_base + kColM + 16 * i, packed);
-        }
-        ptx::tmem_wait_st();
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-        // ---- (f) Yd = M X (A from TMEM) and Sc = B^T Xw
-        if (tid == 0) {
+            // ---- (b) step sizes (the raw value was fetched one chunk ahead), the running
+            //      log2-decay and the column factors of the mask
+            const int64_t t = t0 + tid;
+            const float raw = raw_next;
+            if (c + 1 < c_hi && t + kQ < L)
+                raw_next = __bfloat162float(gdt[(static_cast<int64_t>(b) * L + t + kQ) * H + h]);
+            const float dl = t < L ? step_size<true>(raw, bias, p.softplus) : 0.f;
+            float lam = dl * a_l2;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float v = __shfl_up_sync(0xffffffffu, lam, off);
+                if (lane >= off) lam += v;
+            }
+            // lam of the last step of this warp's 32-step block (before adding earlier warps)
+            const float lam_blk = __shfl_sync(0xffffffffu, lam, 31);
+            if (lane == 31) s_red[warp] = lam;
+            __syncthreads();
+            float base = 0.f;
+            for (int w = 0; w < warp; ++w) base += s_red[w];
+            lam += base;
+            // v_s = exp(Lam_e - Lam_s) dl_s with e the last step of the block holding s
+            s_v[tid] = ex2_approx((base + lam_blk) - lam) * dl;
+            s_dl[tid] = dl;
+            s_lam[tid] = lam;
+
+            if (!wait_all(bar_load, ph_load)) {
+                ok = false;
+                pending = 1;
+                break;
+            }
+            ph_load ^= 1;
+            const float lam_tot = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+
+            // ---- (c) G = C B^T and Yo = C S_in^T
+            if (tid == 0) {
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kN / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kTile + (kk & 3) * 32;
+                    const uint64_t da = ptx::sdesc_sw128(aC + off, 16, 1024);
+                    const uint64_t db = ptx::sdesc_sw128(aB + off, 16, 1024);
+                    ptx::mma_bf16(tmem + kColG, da, db, id_G, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < kN / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kTile + (kk & 3) * 32;
+                    const uint64_t da = ptx::sdesc_sw128(aC + off, 16, 1024);
+                    const uint64_t db = ptx::sdesc_sw128(aW + kk * 2048, 1024, 1024);
+                    ptx::mma_bf16(tmem + kColYo, da, db, id_Yo, kk > 0);
+                }
+                ptx::mma_commit(bar_mma);
+            }
+            if (!wait_all(bar_mma, ph_mma)) {
+                ok = false;
+                pending = 2;
+                break;
+            }
+            ph_mma ^= 1;
             ptx::tc_fence_after();
+
+            // ---- (d) Xw[s, :] = exp(Lam_end - Lam_s) dl_s x_s into sW (S_in is consumed)
+            {
+                const float w = ex2_approx(lam_tot - lam) * dl;
+                const f2 w2{w, w};
 #pragma unroll
-            for (int k = 0; k < kQ / 16; ++k) {
-                const uint64_t db = ptx::sdesc_sw128(aX + k * 2048, 1024, 1024);
-                ptx::mma_bf16_ts(tmem + kColYd, tmem + kColM + 8 * k, db, id_Yd, k > 0);
-            }
-#pragma unroll
-            for (int k = 0; k < kQ / 16; ++k) {
-                const uint64_t da = ptx::sdesc_sw128(aB + k * 2048, kTile, 1024);
-                const uint64_t db = ptx::sdesc_sw128(aW + k * 2048, 1024, 1024);
-                ptx::mma_bf16(tmem + kColSc, da, db, id_Sc, k > 0);
-            }
-            ptx::mma_commit(bar_mma);
-        }
-        if (!wait_all(bar_mma, ph_mma)) {
-            ok = false;
-            pending = 2;
-            break;
-        }
-        ph_mma ^= 1;
-        ptx::tc_fence_after();
-        // ---- (g) state: S <- exp(Lam_end) S + Sc (row n = tid), bf16 copy into sW
-        {
-            const float dec = ex2_approx(lam_tot);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float sc[32];
-                ptx::tmem_ld32(tmem + lane_base + kColSc + 32 * half, sc);
-#pragma unroll
-                for (int pp = 0; pp < 32; ++pp)
-                    S[32 * half + pp] = fmaf(dec, S[32 * half + pp], sc[pp]);
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) st_chunk(sW, tid, q, pack8(S + 8 * q));
-        }
-        // ---- (h) y = Yd + exp(Lam_t) Yo + D x (x gate), written over X in place
-        {
-            const float et = ex2_approx(lam);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float yd[32], yo[32];
-                ptx::tmem_ld32(tmem + lane_base + kColYd + 32 * half, yd);
-                ptx::tmem_ld32(tmem + lane_base + kColYo + 32 * half, yo);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int qq = half * 4 + q;
-                    const uint4 xv = ld_chunk(sX, tid, qq);
-                    const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
-                    uint32_t zin[4] = {0, 0, 0, 0};
-                    if (kGate) {
-                        const uint4 zv = ld_chunk(sZ, tid, qq);
-                        zin[0] = zv.x; zin[1] = zv.y; zin[2] = zv.z; zin[3] = zv.w;
-                    }
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 v = ld_chunk(sX, tid, q);
+                    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
                     uint32_t out[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const f2 xf = ptx::bf2_to_f2(xin[e]);
-                        const int jj = 8 * q + 2 * e;
-                        f2 y = ptx::fma2(f2{et, et}, f2{yo[jj], yo[jj + 1]}, f2{yd[jj], yd[jj + 1]});
-                        y = ptx::fma2(f2{Dh, Dh}, xf, y);
-                        if (kGate) {
-                            const f2 zf = ptx::bf2_to_f2(zin[e]);
-                            y.x *= silu<true>(zf.x);
-                            y.y *= silu<true>(zf.y);
-                        }
-                        out[e] = ptx::f2_to_bf2(y.x, y.y);
+                    for (int i = 0; i < 4; ++i) {
+                        const f2 e = ptx::mul2(ptx::bf2_to_f2(in[i]), w2);
+                        out[i] = ptx::f2_to_bf2(e.x, e.y);
                     }
-                    st_chunk(sX, tid, qq, make_uint4(out[0], out[1], out[2], out[3]));
+                    st_chunk(sW, tid, q, make_uint4(out[0], out[1], out[2], out[3]));
                 }
             }
+            // ---- (e) M[t, s] = G[t, s] exp(Lam_t - Lam_s) dl_s, s <= t, as bf16 pairs over
+            //      G's first 64 columns (row t = tid).  Blocks of 32 columns: below the
+            //      diagonal block exp(Lam_t - Lam_s) = u_t v_s / dl_s with
+            //      u_t = exp(Lam_t - Lam_e), both factors <= 1; on it, pairwise exponentials.
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t packed[16];
+                if (i < warp) {
+                    float gv[32];
+                    ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
+                    const float u = ex2_approx(lam - s_lam[32 * i + 31]);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 vv = *reinterpret_cast<const float2 *>(s_v + 32 * i + 2 * e);
+                        const f2 m = ptx::mul2(ptx::mul2(f2{gv[2 * e], gv[2 * e + 1]}, f2{u, u}),
+                                               f2{vv.x, vv.y});
+                        packed[e] = ptx::f2_to_bf2(m.x, m.y);
+                    }
+                } else if (i == warp) {
+                    float gv[32];
+                    ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float m2[2];
+#pragma unroll
+                        for (int u2 = 0; u2 < 2; ++u2) {
+                            const int s = 32 * i + 2 * e + u2;
+                            const float val = gv[2 * e + u2] * ex2_approx(lam - s_lam[s]) * s_dl[s];
+                            m2[u2] = s <= tid ? val : 0.f;
+                        }
+                        packed[e] = ptx::f2_to_bf2(m2[0], m2[1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) packed[e] = 0u;
+                }
+                ptx::tmem_st16(tmem + lane_base + kColM + 16 * i, packed);
+            }
+            ptx::tmem_wait_st();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            __syncthreads();
+            // ---- (f) Yd = M X (A from TMEM) and Sc = B^T Xw
+            if (tid == 0) {
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kQ / 16; ++kk) {
+                    const uint64_t db = ptx::sdesc_sw128(aX + kk * 2048, 1024, 1024);
+                    ptx::mma_bf16_ts(tmem + kColYd, tmem + kColM + 8 * kk, db, id_Yd, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < kQ / 16; ++kk) {
+                    const uint64_t da = ptx::sdesc_sw128(aB + kk * 2048, kTile, 1024);
+                    const uint64_t db = ptx::sdesc_sw128(aW + kk * 2048, 1024, 1024);
+                    ptx::mma_bf16(tmem + kColSc, da, db, id_Sc, kk > 0);
+                }
+                ptx::mma_commit(bar_mma);
+            }
+            if (!wait_all(bar_mma, ph_mma)) {
+                ok = false;
+                pending = 2;
+                break;
+            }
+            ph_mma ^= 1;
+            ptx::tc_fence_after();
+            // ---- (g) state: S <- exp(Lam_end) S + Sc (row n = tid), bf16 copy into sW
+            {
+                const float dec = ex2_approx(lam_tot);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float sc[32];
+                    ptx::tmem_ld32(tmem + lane_base + kColSc + 32 * half, sc);
+#pragma unroll
+                    for (int pp = 0; pp < 32; ++pp)
+                        S[32 * half + pp] = fmaf(dec, S[32 * half + pp], sc[pp]);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) st_chunk(sW, tid, q, pack8(S + 8 * q));
+            }
+            // ---- (h) y = Yd + exp(Lam_t) Yo + D x (x gate), written over X in place
+            {
+                const float et = ex2_approx(lam);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float yd[32], yo[32];
+                    ptx::tmem_ld32(tmem + lane_base + kColYd + 32 * half, yd);
+                    ptx::tmem_ld32(tmem + lane_base + kColYo + 32 * half, yo);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int qq = half * 4 + q;
+                        const uint4 xv = ld_chunk(sX, tid, qq);
+                        const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
+                        uint32_t zin[4] = {0, 0, 0, 0};
+                        if (kGate) {
+                            const uint4 zv = ld_chunk(sZ, tid, qq);
+                            zin[0] = zv.x; zin[1] = zv.y; zin[2] = zv.z; zin[3] = zv.w;
+                        }
+                        uint32_t out[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const f2 xf = ptx::bf2_to_f2(xin[e]);
+                            const int jj = 8 * q + 2 * e;
+                            f2 y = ptx::fma2(f2{et, et}, f2{yo[jj], yo[jj + 1]},
+                                             f2{yd[jj], yd[jj + 1]});
+                            y = ptx::fma2(f2{Dh, Dh}, xf, y);
+                            if (kGate) {
+                                const f2 zf = ptx::bf2_to_f2(zin[e]);
+                                y.x *= silu<true>(zf.x);
+                                y.y *= silu<true>(zf.y);
+                            }
+                            out[e] = ptx::f2_to_bf2(y.x, y.y);
+                        }
+                        st_chunk(sX, tid, qq, make_uint4(out[0], out[1], out[2], out[3]));
+                    }
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                ptx::tma_store_3d(&maps.Y, sX, h * kP, t0, b);
+                ptx::bulk_commit();
+            }
         }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            ptx::tma_store_3d(&maps.Y, sX, h * kP, t0, b);
-            ptx::bulk_commit();
+        if (!ok) break;
+
+        // ---- the segment's final state: hand it over (head) or write h_final
+        if (kind == 1) {
+            float *dst = sk.states + static_cast<int64_t>(k) * kP * kN;
+#pragma unroll
+            for (int pp = 0; pp < kP; ++pp) __stcg(dst + pp * kN + tid, S[pp]);
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) ptx::st_release_u32(sk.flags + k, 1u);
+        } else if (p.h_final) {
+            float *hf = p.h_final + (static_cast<int64_t>(b) * H + h) * kP * kN;
+#pragma unroll
+            for (int pp = 0; pp < kP; ++pp) hf[pp * kN + tid] = S[pp];
         }
     }
 
@@ -393,11 +480,6 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         if (pending == 2) (void)ptx::mbar_wait(bar_mma, ph_mma);
     }
     if (tid == 0) ptx::bulk_wait<0>();
-    if (ok && p.h_final) {
-        float *hf = p.h_final + (static_cast<int64_t>(b) * H + h) * kP * kN;
-#pragma unroll
-        for (int pp = 0; pp < kP; ++pp) hf[pp * kN + tid] = S[pp];
-    }
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
@@ -436,14 +518,41 @@ bool make_map_sw128(CUtensorMap *m, const void *base, int64_t B, int64_t L, int6
 
 }  // namespace
 
-bool ssd_tc_eligible(const SSDParams &p) {
+bool ssd_tc_sizes_ok(const SSDParams &p) {
     if (!p.io_bf16 || p.headdim != kP || p.dstate != kN) return false;
     if (p.seqlen <= 0 || p.seqlen >= (int64_t(1) << 31)) return false;
-    if (p.nheads > 65535 || p.batch > 65535) return false;
+    return p.batch * p.nheads < (int64_t(1) << 31);
+}
+
+bool ssd_tc_eligible(const SSDParams &p) {
+    if (!ssd_tc_sizes_ok(p)) return false;
     const void *ptrs[] = {p.x, p.Bm, p.Cm, p.z, p.y};
     for (const void *q : ptrs)
         if (q && reinterpret_cast<uintptr_t>(q) % 16 != 0) return false;
     return encoder() != nullptr;
+}
+
+// Persistent grid: two blocks per SM (their TMEM and shared memory fill an SM), but
+// never more blocks than chains.
+int ssd_tc_ctas(const SSDParams &p) {
+    const int64_t chains = p.batch * p.nheads;
+    const int64_t slots = 2 * static_cast<int64_t>(device_sm_count());
+    return static_cast<int>(std::min(chains, slots));
+}
+
+size_t ssd_tc_flag_bytes(const SSDParams &p) {
+    return (static_cast<size_t>(ssd_tc_ctas(p)) * 4 + 255) / 256 * 256;
+}
+
+size_t ssd_workspace_bytes(const SSDParams &p) {
+    size_t bytes = kStatusBytes;
+    if (ssd_tc_sizes_ok(p))
+        bytes += ssd_tc_flag_bytes(p) + static_cast<size_t>(ssd_tc_ctas(p)) * kP * kN * 4;
+    return bytes;
+}
+
+size_t ssd_clear_bytes(const SSDParams &p) {
+    return kStatusBytes + (ssd_tc_sizes_ok(p) ? ssd_tc_flag_bytes(p) : 0);
 }
 
 cudaError_t launch_ssd_tc(const SSDParams &p, cudaStream_t stream) {
@@ -453,20 +562,32 @@ cudaError_t launch_ssd_tc(const SSDParams &p, cudaStream_t stream) {
               make_map_sw128(&m.X, p.x, B, L, H * kP) && make_map_sw128(&m.Y, p.y, B, L, H * kP);
     if (ok && p.z) ok = make_map_sw128(&m.Z, p.z, B, L, H * kP);
     if (!ok) return cudaErrorInvalidValue;
-    dim3 grid(static_cast<unsigned>(H), static_cast<unsigned>(B));
-    cudaError_t e;
-    if (p.z) {
-        e = cudaFuncSetAttribute(ssd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Smem<true>::bytes);
-        if (e != cudaSuccess) return e;
-        ssd_tc_kernel<true><<<grid, kThreads, Smem<true>::bytes, stream>>>(m, p);
-    } else {
-        e = cudaFuncSetAttribute(ssd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Smem<false>::bytes);
-        if (e != cudaSuccess) return e;
-        ssd_tc_kernel<false><<<grid, kThreads, Smem<false>::bytes, stream>>>(m, p);
-    }
-    return cudaGetLastError();
+    Split sk{};
+    sk.nch = static_cast<int>((L + kQ - 1) / kQ);
+    sk.units = B * H * sk.nch;
+    sk.flags = reinterpret_cast<uint32_t *>(p.work);
+    sk.states = reinterpret_cast<float *>(static_cast<char *>(p.work) + ssd_tc_flag_bytes(p));
+    const void *func = p.z ? reinterpret_cast<const void *>(ssd_tc_kernel<true>)
+                           : reinterpret_cast<const void *>(ssd_tc_kernel<false>);
+    const int smem = p.z ? Smem<true>::bytes : Smem<false>::bytes;
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // all of the SM's unified L1/shared storage as shared memory, so that two blocks fit
+    // (the occupancy query below honours this preference)
+    e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    // every block must be resident at once (blocks wait for the state their
+    // predecessor hands over), so launch cooperatively with no more blocks than fit
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    sk.nctas = static_cast<int>(std::min<int64_t>(ssd_tc_ctas(p),
+                                                  static_cast<int64_t>(per_sm) * device_sm_count()));
+    SSDParams pp = p;
+    void *args[] = {&m, &pp, &sk};
+    return cudaLaunchCooperativeKernel(func, dim3(sk.nctas), dim3(kThreads), args, smem, stream);
 }
 
 }  // namespace ssm

@@ -66,8 +66,12 @@ ssm_status check_scan(const ssm_scan_args *a, bool pointers = true) {
 // sizes allow it (pointers that turn out unaligned at call time run the general
 // kernel on the same plan).  The workspace always holds the device status word.
 size_t scan_ws(const ssm_scan_args *a, int64_t *chunk_len, int *nchunks) {
-    const bool tma = ssm::scan_tma_sizes_ok(a->io_dtype == SSM_BF16, a->seqlen, a->dim, a->dstate);
-    ssm::scan_plan(a->batch, a->seqlen, a->dim, a->dstate, a->time_chunk, tma, chunk_len, nchunks);
+    const int bf = a->io_dtype == SSM_BF16;
+    const int tma_warps = ssm::scan_tma_sizes_ok(bf, a->seqlen, a->dim, a->dstate)
+                              ? ssm::scan_tma_block_warps(bf, a->dstate)
+                              : 0;
+    ssm::scan_plan(a->batch, a->seqlen, a->dim, a->dstate, a->time_chunk, tma_warps, chunk_len,
+                   nchunks);
     return ssm::scan_workspace_bytes(a->batch, a->dim, a->dstate, *nchunks);
 }
 
@@ -156,6 +160,34 @@ ssm_status check_decode(const ssm_decode_args *a) {
     const size_t st = (size_t)(a->batch * a->dim * a->dstate) * 4;
     if (overlaps(a->y, tok, a->x, tok) || overlaps(a->y, tok, a->delta, tok) ||
         overlaps(a->y, tok, a->z, tok) || overlaps(a->y, tok, a->state, st))
+        return SSM_ERR_INVALID_ARG;
+    return SSM_OK;
+}
+
+// ------------------------------------------------------------------ multi-head decode
+ssm_status check_ssd_decode(const ssm_ssd_decode_args *a) {
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->batch < 0 || a->nheads < 1 || a->headdim < 1 || a->ngroups < 1 || a->dstate < 1)
+        return SSM_ERR_INVALID_ARG;
+    if (a->nheads % a->ngroups != 0) return SSM_ERR_INVALID_ARG;
+    if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (a->delta_softplus != 0 && a->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (a->dstate > 256) return SSM_ERR_UNSUPPORTED;
+    if (a->batch * a->nheads * a->headdim * 32 > ((int64_t)1 << 40)) return SSM_ERR_UNSUPPORTED;
+    if (a->batch > 0 &&
+        (!a->state || !a->x || !a->delta || !a->B || !a->C || !a->A || !a->y))
+        return SSM_ERR_INVALID_ARG;
+    const size_t e = io_size(a->io_dtype);
+    const void *io_ptrs[] = {a->x, a->delta, a->B, a->C, a->z, a->y};
+    for (const void *p : io_ptrs)
+        if (!aligned(p, e)) return SSM_ERR_ALIGNMENT;
+    const void *f_ptrs[] = {a->state, a->A, a->D, a->delta_bias};
+    for (const void *p : f_ptrs)
+        if (!aligned(p, 4)) return SSM_ERR_ALIGNMENT;
+    const size_t tok = (size_t)(a->batch * a->nheads * a->headdim) * e;
+    const size_t st = (size_t)(a->batch * a->nheads * a->headdim * a->dstate) * 4;
+    if (overlaps(a->y, tok, a->x, tok) || overlaps(a->y, tok, a->z, tok) ||
+        overlaps(a->y, tok, a->state, st))
         return SSM_ERR_INVALID_ARG;
     return SSM_OK;
 }
@@ -271,7 +303,7 @@ ssm_status ssm_ssd_chunk_fwd(const ssm_ssd_args *a, ssm_stream_t stream) {
     if (!a->workspace || a->workspace_bytes < need) return SSM_ERR_WORKSPACE;
     if (a->batch == 0) return SSM_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemsetAsync(a->workspace, 0, kStatusBytes, st);
+    cudaError_t e = cudaMemsetAsync(a->workspace, 0, ssm::ssd_clear_bytes(p), st);
     if (e != cudaSuccess) return SSM_ERR_CUDA;
     return from_cuda(ssm::launch_ssd(p, st));
 }
@@ -297,6 +329,31 @@ ssm_status ssm_step_decode(const ssm_decode_args *a, ssm_stream_t stream) {
     p.bias = a->delta_bias;
     p.y = a->y;
     return from_cuda(ssm::launch_decode(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ssm_status ssm_ssd_step_decode(const ssm_ssd_decode_args *a, ssm_stream_t stream) {
+    ssm_status s = check_ssd_decode(a);
+    if (s != SSM_OK) return s;
+    if (a->batch == 0) return SSM_OK;
+    ssm::SSDDecodeParams p{};
+    p.batch = a->batch;
+    p.nheads = a->nheads;
+    p.headdim = a->headdim;
+    p.ngroups = a->ngroups;
+    p.dstate = a->dstate;
+    p.io_bf16 = a->io_dtype == SSM_BF16;
+    p.softplus = a->delta_softplus;
+    p.state = a->state;
+    p.x = a->x;
+    p.delta = a->delta;
+    p.Bm = a->B;
+    p.Cm = a->C;
+    p.z = a->z;
+    p.A = a->A;
+    p.Dv = a->D;
+    p.bias = a->delta_bias;
+    p.y = a->y;
+    return from_cuda(ssm::launch_ssd_decode(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ssm_status ssm_read_device_status(const void *workspace, ssm_stream_t stream,

@@ -7,10 +7,10 @@
 //
 // B300 mapping: the step is a pure fp32 read-modify-write of the (B, D, N)
 // state plus a few bytes per token, so it is HBM bound (or L2 bound when the
-// state fits in the 126 MB L2).  Each thread owns four consecutive states of one
-// (b, d) row and moves them with one 16-byte load and one 16-byte store; the
-// N / 4 lanes of a row are adjacent, so a warp touches a contiguous 512-byte
-// span, and the readout is reduced with xor shuffles inside those lanes.
+// state fits in the 126 MB L2).  Each thread owns eight (or four) consecutive states
+// of one (b, d) row and moves them with 16-byte loads and stores; the lanes of a row
+// are adjacent, so a warp touches a contiguous 1 KB span, and the readout is reduced
+// with xor shuffles inside those lanes.
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,7 +32,7 @@ __device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16 *p, flo
     v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
 }
 
-template <typename TIO, int LPC, bool kFast, bool kVec>
+template <typename TIO, int NS, int LPC, bool kFast, bool kVec>
 __global__ void __launch_bounds__(kBlock) decode_kernel(DecodeParams p) {
     const TIO *__restrict__ gx = static_cast<const TIO *>(p.x);
     const TIO *__restrict__ gdl = static_cast<const TIO *>(p.delta);
@@ -52,24 +52,29 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(DecodeParams p) {
 
     float acc = 0.f, xv = 0.f;
     if (valid) {
-        xv = Io<TIO>::load(gx + row);
-        const float bias = p.bias ? __ldg(p.bias + d) : 0.f;
-        const float dl = step_size<kFast>(Io<TIO>::load(gdl + row), bias, p.softplus);
-        const float dx = dl * xv;
-        const int n0 = j * 4;
+        const int n0 = j * NS;
         float *st = p.state + row * N + n0;
-        float h[4], a[4], bv[4], cv[4];
+        float h[NS], a[NS], bv[NS], cv[NS];
+        // issue the state loads first: they are the long-latency HBM traffic
         if (kVec) {
-            // whole rows of four states: 16-byte state and A accesses, 8- or 16-byte B, C
-            const float4 s4 = *reinterpret_cast<const float4 *>(st);
-            h[0] = s4.x; h[1] = s4.y; h[2] = s4.z; h[3] = s4.w;
-            const float4 a4 = __ldg(reinterpret_cast<const float4 *>(p.A + d * N + n0));
-            a[0] = a4.x; a[1] = a4.y; a[2] = a4.z; a[3] = a4.w;
-            load4<TIO>(gB + b * N + n0, bv);
-            load4<TIO>(gC + b * N + n0, cv);
+#pragma unroll
+            for (int k = 0; k < NS; k += 4) {
+                const float4 s4 = *reinterpret_cast<const float4 *>(st + k);
+                h[k] = s4.x; h[k + 1] = s4.y; h[k + 2] = s4.z; h[k + 3] = s4.w;
+            }
+#pragma unroll
+            for (int k = 0; k < NS; k += 4) {
+                const float4 a4 = __ldg(reinterpret_cast<const float4 *>(p.A + d * N + n0 + k));
+                a[k] = a4.x; a[k + 1] = a4.y; a[k + 2] = a4.z; a[k + 3] = a4.w;
+                float t4[4];
+                load4<TIO>(gB + b * N + n0 + k, t4);
+                bv[k] = t4[0]; bv[k + 1] = t4[1]; bv[k + 2] = t4[2]; bv[k + 3] = t4[3];
+                load4<TIO>(gC + b * N + n0 + k, t4);
+                cv[k] = t4[0]; cv[k + 1] = t4[1]; cv[k + 2] = t4[2]; cv[k + 3] = t4[3];
+            }
         } else {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < NS; ++k) {
                 const bool in = n0 + k < N;
                 h[k] = in ? st[k] : 0.f;
                 a[k] = in ? __ldg(p.A + d * N + n0 + k) : 0.f;
@@ -77,17 +82,23 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(DecodeParams p) {
                 cv[k] = in ? Io<TIO>::load(gC + b * N + n0 + k) : 0.f;
             }
         }
+        xv = Io<TIO>::load(gx + row);
+        const float bias = p.bias ? __ldg(p.bias + d) : 0.f;
+        const float dl = step_size<kFast>(Io<TIO>::load(gdl + row), bias, p.softplus);
+        const float dx = dl * xv;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < NS; ++k) {
             const float da = decay<kFast>(dl, scale_A<kFast>(a[k]));
             h[k] = fmaf(da, h[k], dx * bv[k]);
             acc = fmaf(cv[k], h[k], acc);
         }
         if (kVec) {
-            *reinterpret_cast<float4 *>(st) = make_float4(h[0], h[1], h[2], h[3]);
+#pragma unroll
+            for (int k = 0; k < NS; k += 4)
+                *reinterpret_cast<float4 *>(st + k) = make_float4(h[k], h[k + 1], h[k + 2], h[k + 3]);
         } else {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
+            for (int k = 0; k < NS; ++k)
                 if (n0 + k < N) st[k] = h[k];
         }
     }
@@ -100,12 +111,12 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(DecodeParams p) {
     }
 }
 
-template <typename TIO, int LPC>
+template <typename TIO, int NS, int LPC>
 cudaError_t launch_lpc(const DecodeParams &p, cudaStream_t stream) {
     constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
-    // the vector path needs whole rows of four states and aligned row starts
+    // the vector path needs whole rows of NS-state slots and aligned row starts
     const size_t e = sizeof(TIO);
-    const bool vec = (p.dstate == 4 * LPC) &&
+    const bool vec = (p.dstate == NS * LPC) &&
                      (reinterpret_cast<uintptr_t>(p.state) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(p.A) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(p.Bm) % (4 * e) == 0) &&
@@ -113,19 +124,21 @@ cudaError_t launch_lpc(const DecodeParams &p, cudaStream_t stream) {
     const int64_t threads = p.batch * p.dim * LPC;
     const unsigned grid = static_cast<unsigned>((threads + kBlock - 1) / kBlock);
     if (vec)
-        decode_kernel<TIO, LPC, kFast, true><<<grid, kBlock, 0, stream>>>(p);
+        decode_kernel<TIO, NS, LPC, kFast, true><<<grid, kBlock, 0, stream>>>(p);
     else
-        decode_kernel<TIO, LPC, kFast, false><<<grid, kBlock, 0, stream>>>(p);
+        decode_kernel<TIO, NS, LPC, kFast, false><<<grid, kBlock, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
+// Eight states per thread where N allows (two 16-byte state accesses in flight per
+// thread keep more HBM traffic outstanding), four otherwise.
 template <typename TIO> cudaError_t launch_typed(const DecodeParams &p, cudaStream_t stream) {
     const int64_t N = p.dstate;
-    if (N <= 4) return launch_lpc<TIO, 1>(p, stream);
-    if (N <= 8) return launch_lpc<TIO, 2>(p, stream);
-    if (N <= 16) return launch_lpc<TIO, 4>(p, stream);
-    if (N <= 32) return launch_lpc<TIO, 8>(p, stream);
-    return launch_lpc<TIO, 16>(p, stream);
+    if (N <= 4) return launch_lpc<TIO, 4, 1>(p, stream);
+    if (N <= 8) return launch_lpc<TIO, 8, 1>(p, stream);
+    if (N <= 16) return launch_lpc<TIO, 8, 2>(p, stream);
+    if (N <= 32) return launch_lpc<TIO, 8, 4>(p, stream);
+    return launch_lpc<TIO, 8, 8>(p, stream);
 }
 
 }  // namespace

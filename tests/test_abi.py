@@ -184,6 +184,23 @@ def test_decode_rejects_bad_arguments(lib):
     assert rc(batch=0) == OK
 
 
+def test_ssd_decode_rejects_bad_arguments(lib):
+    def rc(**kw):
+        base = dict(batch=2, nheads=4, headdim=64, ngroups=1, dstate=128, io_dtype=1,
+                    delta_softplus=1, state=0x100000, x=0x200000, delta=0x300000, B=0x400000,
+                    C=0x500000, z=None, A=0x600000, D=None, delta_bias=None, y=0x700000)
+        base.update(kw)
+        a = bd.SSDDecodeArgs(**base)
+        return lib.ssm_ssd_step_decode(ctypes.byref(a), None)
+    assert lib.ssm_ssd_step_decode(None, None) == INVALID
+    assert rc(ngroups=3) == INVALID                  # H % G != 0
+    assert rc(dstate=300) == UNSUPPORTED
+    assert rc(state=None) == INVALID
+    assert rc(x=0x200001) == ALIGN
+    assert rc(y=0x200000) == INVALID                 # y aliases x
+    assert rc(batch=0) == OK                         # nothing to do, nothing launched
+
+
 def test_ops_fail_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(bd, "_lib", None)
     monkeypatch.setattr(bd, "_LIB_PATH", str(tmp_path / "missing.so"))

@@ -360,3 +360,38 @@ def test_oracle_runs_threaded_identically():
     y4, h4 = oracle.scan(**p.oracle_args(), threads=4)
     np.testing.assert_array_equal(y1, y4)
     np.testing.assert_array_equal(h1, h4)
+
+
+# ---------------------------------------------------------------- multi-head decode step
+def test_ssd_decode_steps_equal_ssd_scan():
+    """L single-token steps of the multi-head recurrence equal the (pinned) SSD oracle
+    over the same L tokens, outputs and final state, with groups and a gate."""
+    p = _ssd_small(11, nb=2, L=13, H=4, P=3, G=2, N=5, gate=True, h0=True)
+    y_ref, h_ref = oracle.ssd(**p.oracle_args())
+    state = p.h0.astype(np.float64).copy()
+    ys = []
+    for t in range(p.seqlen):
+        ys.append(oracle.ssd_decode_step(state, p.x[:, t], p.delta[:, t], p.A, p.B[:, t],
+                                         p.C[:, t], Dv=p.D, z=p.z[:, t], bias=p.bias,
+                                         softplus=p.softplus))
+    np.testing.assert_allclose(np.stack(ys, axis=1), y_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(state, h_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_ssd_decode_zero_step_keeps_state():
+    """dl = 0 exactly (raw 0, no bias, no softplus): the state is unchanged and
+    y = S C + D x (no gate)."""
+    rng = _rng(12)
+    nb, H, P, G, N = 2, 4, 3, 2, 5
+    state = rng.standard_normal((nb, H, P, N))
+    s0 = state.copy()
+    x = rng.standard_normal((nb, H, P))
+    Bm = rng.standard_normal((nb, G, N))
+    Cm = rng.standard_normal((nb, G, N))
+    A = -rng.uniform(1, 16, H)
+    Dv = rng.standard_normal(H)
+    y = oracle.ssd_decode_step(state, x, np.zeros((nb, H)), A, Bm, Cm, Dv=Dv, softplus=False)
+    np.testing.assert_array_equal(state, s0)
+    g = np.arange(H) // (H // G)
+    expect = np.einsum("bhpn,bhn->bhp", s0, Cm[:, g]) + Dv[None, :, None] * x
+    np.testing.assert_allclose(y, expect, rtol=1e-13, atol=1e-13)

@@ -48,6 +48,14 @@ def test_tensor_core_path(L, nb, H, G, gate, h0):
     _check(p)
 
 
+def test_tensor_core_chains_split_between_blocks():
+    """More (batch, head) chains than resident blocks: the persistent grid cuts chains
+    between blocks and hands the state over through the workspace."""
+    p = W.ssd_problem(1, 300, 320, 64, 1, 128, chunk=128, io="bf16", seed=91, h0=True)
+    assert _uses_tc(p)
+    _check(p)
+
+
 def test_tensor_core_path_is_not_taken_for_other_shapes():
     assert not _uses_tc(W.ssd_problem(1, 64, 2, 32, 1, 128, io="bf16", seed=1))
     assert not _uses_tc(W.ssd_problem(1, 64, 2, 64, 1, 64, io="bf16", seed=1))
