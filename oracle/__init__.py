@@ -48,13 +48,13 @@ def _load():
     dp = ctypes.POINTER(ctypes.c_double)
     i64 = ctypes.c_int64
     lib.oracle_scan_f64.restype = ctypes.c_int
-    lib.oracle_scan_f64.argtypes = [i64, i64, i64, i64] + [dp] * 8 + [ctypes.c_int, dp, dp, dp,
-                                                                    ctypes.c_int]
+    lib.oracle_scan_f64.argtypes = [i64, i64, i64, i64] + [dp] * 8 + [ctypes.c_int, ctypes.c_int,
+                                                                    dp, dp, dp, ctypes.c_int]
     lib.oracle_ssd_f64.restype = ctypes.c_int
     lib.oracle_ssd_f64.argtypes = [i64] * 6 + [dp] * 8 + [ctypes.c_int, dp, dp, dp, ctypes.c_int]
     lib.oracle_decode_f64.restype = ctypes.c_int
-    lib.oracle_decode_f64.argtypes = [i64, i64, i64, dp] + [dp] * 8 + [ctypes.c_int, dp,
-                                                                    ctypes.c_int]
+    lib.oracle_decode_f64.argtypes = [i64, i64, i64, dp] + [dp] * 8 + [ctypes.c_int, ctypes.c_int,
+                                                                    dp, ctypes.c_int]
     lib.oracle_ssd_decode_f64.restype = ctypes.c_int
     lib.oracle_ssd_decode_f64.argtypes = [i64] * 5 + [dp] * 9 + [ctypes.c_int, dp, ctypes.c_int]
     lib.oracle_softplus_f64.restype = ctypes.c_double
@@ -85,9 +85,10 @@ def softplus(v: float) -> float:
 
 
 def scan(x, delta, A, Bm, Cm, Dv=None, z=None, bias=None, softplus: bool = True,
-         h0=None, threads: Optional[int] = None):
+         h0=None, threads: Optional[int] = None, zoh: bool = False):
     """Sequential S6 scan.  x, delta, z: (B,L,D); Bm, Cm: (B,L,N); A: (D,N);
-    Dv, bias: (D,); h0: (B,D,N).  Returns (y (B,L,D), h_final (B,D,N))."""
+    Dv, bias: (D,); h0: (B,D,N).  zoh selects the zero-order-hold input coefficient
+    (exp(dl A) - 1) / A instead of dl.  Returns (y (B,L,D), h_final (B,D,N))."""
     lib = _load()
     x, delta, A, Bm, Cm = map(_f64, (x, delta, A, Bm, Cm))
     Dv, z, bias, h0 = map(_f64, (Dv, z, bias, h0))
@@ -98,8 +99,8 @@ def scan(x, delta, A, Bm, Cm, Dv=None, z=None, bias=None, softplus: bool = True,
     y = np.empty((nb, L, D), np.float64)
     hf = np.empty((nb, D, N), np.float64)
     rc = lib.oracle_scan_f64(nb, L, D, N, _ptr(x), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm),
-                             _ptr(Dv), _ptr(z), _ptr(bias), int(bool(softplus)), _ptr(h0),
-                             _ptr(y), _ptr(hf), threads or default_threads())
+                             _ptr(Dv), _ptr(z), _ptr(bias), int(bool(softplus)), int(bool(zoh)),
+                             _ptr(h0), _ptr(y), _ptr(hf), threads or default_threads())
     if rc != 0:
         raise RuntimeError(f"oracle_scan_f64 failed: {rc}")
     return y, hf
@@ -128,7 +129,7 @@ def ssd(x, delta, A, Bm, Cm, Dv=None, z=None, bias=None, softplus: bool = True,
 
 
 def decode_step(state, x, delta, A, Bm, Cm, Dv=None, z=None, bias=None,
-                softplus: bool = True, threads: Optional[int] = None):
+                softplus: bool = True, threads: Optional[int] = None, zoh: bool = False):
     """One recurrent step.  state: (B,D,N) float64, UPDATED IN PLACE (it must
     already be a C-contiguous float64 array); x, delta, z: (B,D); Bm, Cm: (B,N);
     A: (D,N); Dv, bias: (D,).  Returns y (B,D)."""
@@ -143,7 +144,7 @@ def decode_step(state, x, delta, A, Bm, Cm, Dv=None, z=None, bias=None,
     y = np.empty((nb, D), np.float64)
     rc = lib.oracle_decode_f64(nb, D, N, _ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(Bm),
                                _ptr(Cm), _ptr(Dv), _ptr(z), _ptr(bias), int(bool(softplus)),
-                               _ptr(y), threads or default_threads())
+                               int(bool(zoh)), _ptr(y), threads or default_threads())
     if rc != 0:
         raise RuntimeError(f"oracle_decode_f64 failed: {rc}")
     return y

@@ -23,7 +23,8 @@
  *     head with a scalar decay per head and B, C shared by the heads of a group.
  *
  * Readings where the pages are silent or garbled (all listed in the design
- * notes): Δ is per channel; B̄ = ΔB; y = (C·h + D·x)·silu(z); the initial state
+ * notes): Δ is per channel; B̄ = ΔB (the simplified form; the zero-order-hold form
+ * (exp(ΔA) - I) A^-1 B of section "이산화" on request); y = (C·h + D·x)·silu(z); the initial state
  * is zero unless given; softplus(v) = log(1 + e^v) evaluated in the overflow-
  * free form max(v,0) + log1p(exp(-|v|)).
  *
@@ -64,10 +65,20 @@ static double step_size(double raw, const double *bias, int64_t c, int softplus)
     return softplus ? softplus_f64(v) : v;
 }
 
+/* Input coefficient of the discretised recurrence for one state with diagonal entry a:
+ *   Euler (the simplified form, tildalice "Δ의 직관적 이해"):  dl
+ *   zero-order hold (tildalice "이산화"):  (exp(dl a) - 1) / a, whose limit as a -> 0
+ *   is dl; B̄ x = coefficient * B * x. */
+static double input_coef(double dl, double a, int zoh)
+{
+    if (!zoh || a == 0.0) return dl;
+    return expm1(dl * a) / a;
+}
+
 int oracle_scan_f64(int64_t nb, int64_t L, int64_t D, int64_t N,
                     const double *x, const double *delta, const double *A,
                     const double *Bm, const double *Cm, const double *Dv,
-                    const double *z, const double *bias, int softplus,
+                    const double *z, const double *bias, int softplus, int zoh,
                     const double *h0, double *y, double *h_final, int nthreads)
 {
     if (nb < 0 || L < 0 || D < 0 || N < 1) return -1;
@@ -84,9 +95,10 @@ int oracle_scan_f64(int64_t nb, int64_t L, int64_t D, int64_t N,
             int64_t bt = b * L + t;
             double xv = x[bt * D + d];
             double dl = step_size(delta[bt * D + d], bias, d, softplus);
-            /* state update: h <- exp(dl*A) h + dl*B_t*x_t */
+            /* state update: h <- exp(dl*A) h + coef*B_t*x_t (coef = dl, or the ZOH one) */
             for (int64_t n = 0; n < N; ++n)
-                h[n] = exp(dl * A[d * N + n]) * h[n] + dl * Bm[bt * N + n] * xv;
+                h[n] = exp(dl * A[d * N + n]) * h[n] +
+                       input_coef(dl, A[d * N + n], zoh) * Bm[bt * N + n] * xv;
             /* readout after the update, then the D skip and the gate */
             double acc = 0.0;
             for (int64_t n = 0; n < N; ++n) acc += Cm[bt * N + n] * h[n];
@@ -148,7 +160,7 @@ int oracle_ssd_f64(int64_t nb, int64_t L, int64_t H, int64_t P, int64_t G, int64
 int oracle_decode_f64(int64_t nb, int64_t D, int64_t N, double *state,
                       const double *x, const double *delta, const double *A,
                       const double *Bm, const double *Cm, const double *Dv,
-                      const double *z, const double *bias, int softplus,
+                      const double *z, const double *bias, int softplus, int zoh,
                       double *y, int nthreads)
 {
     if (nb < 0 || D < 0 || N < 1) return -1;
@@ -161,7 +173,7 @@ int oracle_decode_f64(int64_t nb, int64_t D, int64_t N, double *state,
         double *h = state + c * N;
         double acc = 0.0;
         for (int64_t n = 0; n < N; ++n) {
-            h[n] = exp(dl * A[d * N + n]) * h[n] + dl * Bm[b * N + n] * xv;
+            h[n] = exp(dl * A[d * N + n]) * h[n] + input_coef(dl, A[d * N + n], zoh) * Bm[b * N + n] * xv;
             acc += Cm[b * N + n] * h[n];
         }
         double out = acc + (Dv ? Dv[d] : 0.0) * xv;

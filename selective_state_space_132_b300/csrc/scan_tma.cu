@@ -50,7 +50,10 @@ namespace {
 using ptx::f2;
 
 constexpr int kT = 32;       // time steps per tile (one per lane in prologue/epilogue)
-constexpr int kStages = 2;   // TMA pipeline depth
+#ifndef SSM_SCAN_STAGES
+#define SSM_SCAN_STAGES 2
+#endif
+constexpr int kStages = SSM_SCAN_STAGES;  // TMA pipeline depth
 #ifndef SSM_SCAN_UNROLL
 #define SSM_SCAN_UNROLL 4
 #endif

@@ -103,11 +103,14 @@ __device__ __forceinline__ uint4 pack8(const float *v) {
 // block k + 1 runs its other work first and that chain's tail last, after
 // acquiring the flag.  With at least one chain per block a chain is cut at most
 // once and, since head + tail = nch <= the steps of a block, no block waits in
-// steady state.
+// steady state.  A block takes its range index k from an atomic ticket, i.e. in the
+// order blocks actually start, so the block it may wait for (k - 1) has always started
+// already and the wait cannot depend on a block that is not yet resident.
 struct Split {
     int nctas;
     int nch;           // chunks per chain
     int64_t units;
+    uint32_t *ticket;  // block-order counter, zeroed before the launch
     uint32_t *flags;   // nctas flags, zeroed before the launch
     float *states;     // nctas states of P x N fp32
 };
@@ -129,7 +132,6 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int k = blockIdx.x;
     const int64_t H = p.nheads, L = p.seqlen;
     const __nv_bfloat16 *gdt = static_cast<const __nv_bfloat16 *>(p.delta);
     DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
@@ -149,11 +151,14 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         ptx::tmem_alloc(s_tmem, kTmemCols);
         ptx::tmem_relinquish();
     }
+    if (tid == 0) reinterpret_cast<volatile uint32_t *>(s_red)[0] = atomicAdd(sk.ticket, 1u);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int k = static_cast<int>(reinterpret_cast<volatile uint32_t *>(s_red)[0]);
+    __syncthreads();  // s_red is reused for the warp totals
 
     const uint32_t id_G = ptx::idesc_bf16(128, 128, 0, 0);
     const uint32_t id_Yo = ptx::idesc_bf16(128, kP, 0, 1);
@@ -540,8 +545,9 @@ int ssd_tc_ctas(const SSDParams &p) {
     return static_cast<int>(std::min(chains, slots));
 }
 
+// ticket + one hand-over flag per block
 size_t ssd_tc_flag_bytes(const SSDParams &p) {
-    return (static_cast<size_t>(ssd_tc_ctas(p)) * 4 + 255) / 256 * 256;
+    return (static_cast<size_t>(ssd_tc_ctas(p) + 1) * 4 + 255) / 256 * 256;
 }
 
 size_t ssd_workspace_bytes(const SSDParams &p) {
@@ -565,7 +571,8 @@ cudaError_t launch_ssd_tc(const SSDParams &p, cudaStream_t stream) {
     Split sk{};
     sk.nch = static_cast<int>((L + kQ - 1) / kQ);
     sk.units = B * H * sk.nch;
-    sk.flags = reinterpret_cast<uint32_t *>(p.work);
+    sk.ticket = reinterpret_cast<uint32_t *>(p.work);
+    sk.flags = sk.ticket + 1;
     sk.states = reinterpret_cast<float *>(static_cast<char *>(p.work) + ssd_tc_flag_bytes(p));
     const void *func = p.z ? reinterpret_cast<const void *>(ssd_tc_kernel<true>)
                            : reinterpret_cast<const void *>(ssd_tc_kernel<false>);
@@ -573,21 +580,15 @@ cudaError_t launch_ssd_tc(const SSDParams &p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // all of the SM's unified L1/shared storage as shared memory, so that two blocks fit
-    // (the occupancy query below honours this preference)
     e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    // every block must be resident at once (blocks wait for the state their
-    // predecessor hands over), so launch cooperatively with no more blocks than fit
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, kThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    sk.nctas = static_cast<int>(std::min<int64_t>(ssd_tc_ctas(p),
-                                                  static_cast<int64_t>(per_sm) * device_sm_count()));
-    SSDParams pp = p;
-    void *args[] = {&m, &pp, &sk};
-    return cudaLaunchCooperativeKernel(func, dim3(sk.nctas), dim3(kThreads), args, smem, stream);
+    // two blocks per SM (their TMEM, shared memory and registers fill it); the ticket
+    // keeps the hand-over waits safe whatever the hardware keeps resident
+    sk.nctas = ssd_tc_ctas(p);
+    auto kern = p.z ? ssd_tc_kernel<true> : ssd_tc_kernel<false>;
+    kern<<<sk.nctas, kThreads, smem, stream>>>(m, p, sk);
+    return cudaGetLastError();
 }
 
 }  // namespace ssm

@@ -91,6 +91,7 @@ class ScanProblem:
     bias: Optional[np.ndarray]
     softplus: bool
     h0: Optional[np.ndarray]
+    zoh: bool = False  # zero-order-hold input coefficient instead of dl
 
     @property
     def updates(self) -> int:
@@ -98,7 +99,7 @@ class ScanProblem:
 
     def oracle_args(self) -> Dict[str, object]:
         return dict(x=self.x, delta=self.delta, A=self.A, Bm=self.B, Cm=self.C, Dv=self.D,
-                    z=self.z, bias=self.bias, softplus=self.softplus, h0=self.h0)
+                    z=self.z, bias=self.bias, softplus=self.softplus, h0=self.h0, zoh=self.zoh)
 
 
 def scan_problem(batch: int, seqlen: int, dim: int, dstate: int, io: str = "bf16",
