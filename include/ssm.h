@@ -85,7 +85,11 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
  * Workspace: ssm_scan_workspace_size() bytes (it reads only the sizes and flags of
  * `args`, not the pointers), 256-byte aligned, always required: its first 256 bytes
  * hold the device status word (cleared by the call itself), the rest the chunk
- * summaries of a time-split sequence; contents need no initialisation. */
+ * summaries of a time-split sequence; contents need no initialisation.
+ * discretization: SSM_DISC_EULER (0, B̄ = dl B: the simplified form of the tildalice
+ * review, section "Δ의 직관적 이해") or SSM_DISC_ZOH (1, zero-order hold:
+ * B̄ = (exp(dl A) - 1) / A B, section "이산화"; the A -> 0 limit is dl B). */
+typedef enum { SSM_DISC_EULER = 0, SSM_DISC_ZOH = 1 } ssm_discretization;
 typedef struct {
     int64_t batch, seqlen, dim, dstate;
     int64_t time_chunk;
@@ -97,6 +101,8 @@ typedef struct {
     float *h_final;
     void *workspace;
     size_t workspace_bytes;
+    int32_t discretization; /* ssm_discretization */
+    int32_t reserved;       /* 0 */
 } ssm_scan_args;
 
 SSM_API ssm_status ssm_scan_workspace_size(const ssm_scan_args *args, size_t *bytes);
@@ -169,7 +175,7 @@ SSM_API ssm_status ssm_ssd_plan(const ssm_ssd_args *args, int32_t *tensor_core);
  *   A : (D, N) fp32                    D, delta_bias : (D) fp32
  * Nullable: D, delta_bias, z.  One call advances every sequence by one token;
  * calls on one stream are ordered, so L calls equal one ssm_scan_fwd over L steps
- * (up to rounding).  No workspace. */
+ * (up to rounding) with the same discretization.  No workspace. */
 typedef struct {
     int64_t batch, dim, dstate;
     int32_t io_dtype;
@@ -178,6 +184,8 @@ typedef struct {
     const void *x, *delta, *B, *C, *z;
     const float *A, *D, *delta_bias;
     void *y;
+    int32_t discretization; /* ssm_discretization */
+    int32_t reserved;       /* 0 */
 } ssm_decode_args;
 
 SSM_API ssm_status ssm_step_decode(const ssm_decode_args *args, ssm_stream_t stream);
@@ -204,6 +212,27 @@ typedef struct {
 } ssm_ssd_decode_args;
 
 SSM_API ssm_status ssm_ssd_step_decode(const ssm_ssd_decode_args *args, ssm_stream_t stream);
+
+/* ------------------------------------------------------------------ causal conv1d + SiLU
+ * The Conv1D (kernel K) + SiLU step in front of the selective scan in the Mamba block
+ * (tildalice review, section "Mamba 블록 아키텍처" and its reference class: a depthwise
+ * Conv1D with K - 1 steps of left padding, cropped to L, then SiLU):
+ *   out[b, t, d] = silu( bias_d + sum_{k<K} weight[d, k] x[b, t - (K-1) + k, d] )
+ * x at t < 0 comes from x_prev (the K - 1 inputs just before this call, oldest first),
+ * or is zero when x_prev is NULL, so a sequence can be processed in pieces.
+ * Shapes: x, out (B, L, D) io_dtype; x_prev (B, K - 1, D) io_dtype; weight (D, K) fp32;
+ * bias (D) fp32.  Nullable: bias, x_prev.  1 <= K <= 8; silu 0 returns the
+ * convolution alone.  out may not alias x or x_prev.  No workspace. */
+typedef struct {
+    int64_t batch, seqlen, dim, width;
+    int32_t io_dtype;
+    int32_t silu;
+    const void *x, *x_prev;
+    const float *weight, *bias;
+    void *out;
+} ssm_conv1d_args;
+
+SSM_API ssm_status ssm_conv1d(const ssm_conv1d_args *args, ssm_stream_t stream);
 
 /* ------------------------------------------------------------------ utilities */
 SSM_API const char *ssm_status_string(ssm_status status);

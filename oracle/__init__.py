@@ -57,6 +57,8 @@ def _load():
                                                                     dp, ctypes.c_int]
     lib.oracle_ssd_decode_f64.restype = ctypes.c_int
     lib.oracle_ssd_decode_f64.argtypes = [i64] * 5 + [dp] * 9 + [ctypes.c_int, dp, ctypes.c_int]
+    lib.oracle_conv1d_f64.restype = ctypes.c_int
+    lib.oracle_conv1d_f64.argtypes = [i64] * 4 + [dp] * 4 + [ctypes.c_int, dp, ctypes.c_int]
     lib.oracle_softplus_f64.restype = ctypes.c_double
     lib.oracle_softplus_f64.argtypes = [ctypes.c_double]
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -172,6 +174,26 @@ def ssd_decode_step(state, x, delta, A, Bm, Cm, Dv=None, z=None, bias=None,
     if rc != 0:
         raise RuntimeError(f"oracle_ssd_decode_f64 failed: {rc}")
     return y
+
+
+def conv1d(x, w, bias=None, x_prev=None, silu: bool = True, threads: Optional[int] = None):
+    """Causal depthwise convolution along time (kernel K, K-1 steps of left padding, or
+    the carried-in x_prev (B, K-1, D)), then SiLU.  x: (B,L,D); w: (D,K); bias: (D,).
+    Returns (B,L,D)."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    bias, x_prev = _f64(bias), _f64(x_prev)
+    nb, L, D = x.shape
+    K = w.shape[1]
+    assert w.shape == (D, K)
+    if x_prev is not None:
+        assert x_prev.shape == (nb, K - 1, D)
+    out = np.empty((nb, L, D), np.float64)
+    rc = lib.oracle_conv1d_f64(nb, L, D, K, _ptr(x), _ptr(w), _ptr(bias), _ptr(x_prev),
+                               int(bool(silu)), _ptr(out), threads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_conv1d_f64 failed: {rc}")
+    return out
 
 
 def rel_l2(a, b) -> float:

@@ -220,6 +220,37 @@ int oracle_ssd_decode_f64(int64_t nb, int64_t H, int64_t P, int64_t G, int64_t N
     return 0;
 }
 
+/* Causal depthwise convolution along time, then SiLU (tildalice review, section
+ * "Mamba 블록 아키텍처" and its reference class: a depthwise Conv1D of kernel K with
+ * K - 1 steps of left padding, cropped to L, followed by SiLU):
+ *   pre[b,t,d] = bias[d] + sum_{k=0}^{K-1} w[d,k] x[b, t-(K-1)+k, d]
+ *   out[b,t,d] = silu(pre) (or pre when silu == 0)
+ * x at t < 0 comes from x_prev (B, K-1, D) (the K-1 inputs just before this call, oldest
+ * first) or is zero.  Layouts: x, out (B,L,D); w (D,K); bias (D). */
+int oracle_conv1d_f64(int64_t nb, int64_t L, int64_t D, int64_t K, const double *x,
+                      const double *w, const double *bias, const double *x_prev, int silu,
+                      double *out, int nthreads)
+{
+    if (nb < 0 || L < 0 || D < 0 || K < 1) return -1;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int64_t c = 0; c < nb * D; ++c) {
+        int64_t b = c / D, d = c % D;
+        for (int64_t t = 0; t < L; ++t) {
+            double acc = bias ? bias[d] : 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                int64_t s = t - (K - 1) + k;
+                double xv;
+                if (s >= 0) xv = x[(b * L + s) * D + d];
+                else xv = x_prev ? x_prev[(b * (K - 1) + (K - 1 + s)) * D + d] : 0.0;
+                acc += w[d * K + k] * xv;
+            }
+            out[(b * L + t) * D + d] = silu ? silu_f64(acc) : acc;
+        }
+    }
+    return 0;
+}
+
 /* Helper exposed for the pins: the scalar softplus used above. */
 double oracle_softplus_f64(double v) { return softplus_f64(v); }
 

@@ -18,7 +18,8 @@ _STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED",
 
 EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
             "ssm_ssd_workspace_size", "ssm_ssd_chunk_fwd", "ssm_ssd_plan", "ssm_step_decode",
-            "ssm_ssd_step_decode", "ssm_status_string", "ssm_version", "ssm_check_bounded_wait",
+            "ssm_ssd_step_decode", "ssm_conv1d", "ssm_status_string", "ssm_version",
+            "ssm_check_bounded_wait",
             "ssm_read_device_status"]
 
 _i64, _i32, _vp, _fp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p
@@ -30,7 +31,8 @@ class ScanArgs(ctypes.Structure):
                 ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp), ("z", _vp),
                 ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("h0", _fp),
                 ("y", _vp), ("h_final", _fp), ("workspace", _vp),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("discretization", _i32),
+                ("reserved", _i32)]
 
 
 class SSDArgs(ctypes.Structure):
@@ -47,7 +49,23 @@ class DecodeArgs(ctypes.Structure):
     _fields_ = [("batch", _i64), ("dim", _i64), ("dstate", _i64),
                 ("io_dtype", _i32), ("delta_softplus", _i32), ("state", _fp),
                 ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp), ("z", _vp),
-                ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("y", _vp)]
+                ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("y", _vp),
+                ("discretization", _i32), ("reserved", _i32)]
+
+
+class Conv1dArgs(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("seqlen", _i64), ("dim", _i64), ("width", _i64),
+                ("io_dtype", _i32), ("silu", _i32), ("x", _vp), ("x_prev", _vp),
+                ("weight", _fp), ("bias", _fp), ("out", _vp)]
+
+
+DISCRETIZATIONS = {"euler": 0, "zoh": 1}
+
+
+def _disc(name: str) -> int:
+    if name not in DISCRETIZATIONS:
+        raise ValueError(f"discretization must be one of {sorted(DISCRETIZATIONS)}")
+    return DISCRETIZATIONS[name]
 
 
 class SSDDecodeArgs(ctypes.Structure):
@@ -99,6 +117,8 @@ def load_library():
     lib.ssm_step_decode.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
     lib.ssm_ssd_step_decode.argtypes = [ctypes.POINTER(SSDDecodeArgs), _vp]
     lib.ssm_ssd_step_decode.restype = ctypes.c_int
+    lib.ssm_conv1d.argtypes = [ctypes.POINTER(Conv1dArgs), _vp]
+    lib.ssm_conv1d.restype = ctypes.c_int
     lib.ssm_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
     lib.ssm_check_bounded_wait.argtypes = [_vp, ctypes.c_int64, _vp]
     lib.ssm_check_bounded_wait.restype = ctypes.c_int
@@ -168,7 +188,7 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
 
 # ---------------------------------------------------------------- scan
 def _scan_args(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final,
-               time_chunk) -> ScanArgs:
+               time_chunk, discretization: str = "euler") -> ScanArgs:
     nb, L, Dm = x.shape
     N = A.shape[1]
     dev, io = x.device, x.dtype
@@ -185,9 +205,11 @@ def _scan_args(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_fin
     _check(h_final, "h_final", (nb, Dm, N), torch.float32, dev)
     if not x.is_contiguous():
         raise ValueError("x must be contiguous")
-    return ScanArgs(nb, L, Dm, N, int(time_chunk), _io_code(x), int(bool(delta_softplus)),
-                    _ptr(x), _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
-                    _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(h_final), None, 0)
+    a = ScanArgs(nb, L, Dm, N, int(time_chunk), _io_code(x), int(bool(delta_softplus)),
+                 _ptr(x), _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
+                 _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(h_final), None, 0)
+    a.discretization = _disc(discretization)
+    return a
 
 
 def scan_workspace_size(batch: int, seqlen: int, dim: int, dstate: int,
@@ -224,9 +246,10 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
              h0: Optional[torch.Tensor] = None, return_final_state: bool = True,
              y: Optional[torch.Tensor] = None, h_final: Optional[torch.Tensor] = None,
              workspace: Optional[torch.Tensor] = None, time_chunk: int = 0,
-             stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+             stream=None, discretization: str = "euler") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Selective scan.  x, delta, z: (B, L, D); A: (D, N) fp32; B, C: (B, L, N);
-    D, delta_bias: (D,) fp32; h0: (B, D, N) fp32.  Returns (y, h_final)."""
+    D, delta_bias: (D,) fp32; h0: (B, D, N) fp32; discretization "euler" (B̄ = dl B)
+    or "zoh" (zero-order hold).  Returns (y, h_final)."""
     lib = load_library()
     nb, L, Dm = x.shape
     N = A.shape[1]
@@ -235,7 +258,7 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
     if h_final is None and return_final_state:
         h_final = torch.empty((nb, Dm, N), dtype=torch.float32, device=x.device)
     args = _scan_args(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final,
-                      time_chunk)
+                      time_chunk, discretization)
     need = ctypes.c_size_t(0)
     _raise(lib.ssm_scan_workspace_size(ctypes.byref(args), ctypes.byref(need)),
            "ssm_scan_workspace_size")
@@ -345,7 +368,7 @@ def step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: to
                 B: torch.Tensor, C: torch.Tensor, D: Optional[torch.Tensor] = None,
                 z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
                 delta_softplus: bool = True, y: Optional[torch.Tensor] = None,
-                stream=None) -> torch.Tensor:
+                stream=None, discretization: str = "euler") -> torch.Tensor:
     """One recurrent step; ``state`` (B, D, N) fp32 is updated in place.
     x, delta, z: (B, D); B, C: (B, N); A: (D, N) fp32; D, delta_bias: (D,) fp32."""
     lib = load_library()
@@ -367,6 +390,7 @@ def step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: to
     args = DecodeArgs(nb, Dm, N, _io_code(x), int(bool(delta_softplus)), _ptr(state), _ptr(x),
                       _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
                       _ptr(delta_bias), _ptr(y))
+    args.discretization = _disc(discretization)
     _raise(lib.ssm_step_decode(ctypes.byref(args), _stream(stream)), "ssm_step_decode")
     return y
 
@@ -402,3 +426,28 @@ def ssd_step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A
                          _ptr(delta_bias), _ptr(y))
     _raise(lib.ssm_ssd_step_decode(ctypes.byref(args), _stream(stream)), "ssm_ssd_step_decode")
     return y
+
+
+# ---------------------------------------------------------------- causal conv1d + SiLU
+def conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
+           x_prev: Optional[torch.Tensor] = None, silu: bool = True,
+           out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal depthwise convolution along time, then SiLU.  x: (B, L, D); weight: (D, K)
+    fp32; bias: (D,) fp32; x_prev: (B, K-1, D), the inputs just before x (zeros when
+    None).  Returns (B, L, D) in x's dtype."""
+    lib = load_library()
+    nb, L, Dm = x.shape
+    K = weight.shape[1]
+    dev, io = x.device, x.dtype
+    _io_code(x)
+    _check(x, "x", (nb, L, Dm), io, dev)
+    _check(weight, "weight", (Dm, K), torch.float32, dev)
+    _check(bias, "bias", (Dm,), torch.float32, dev)
+    _check(x_prev, "x_prev", (nb, K - 1, Dm), io, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    _check(out, "out", (nb, L, Dm), io, dev)
+    args = Conv1dArgs(nb, L, Dm, K, _io_code(x), int(bool(silu)), _ptr(x), _ptr(x_prev),
+                      _ptr(weight), _ptr(bias), _ptr(out))
+    _raise(lib.ssm_conv1d(ctypes.byref(args), _stream(stream)), "ssm_conv1d")
+    return out

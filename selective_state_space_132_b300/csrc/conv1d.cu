@@ -1,0 +1,162 @@
+// Causal depthwise convolution along time with an optional SiLU: the Conv1D (k = 4) +
+// SiLU step in front of the selective scan in the block of the tildalice review
+// (section "Mamba 블록 아키텍처" and its reference class: a depthwise Conv1D with K - 1
+// steps of left padding, cropped to L):
+//   out[b, t, d] = silu( bias_d + sum_{k<K} w[d, k] x[b, t - (K-1) + k, d] )
+// with x at t < 0 taken from x_prev (the K - 1 inputs just before this call) or zero.
+//
+// B300 mapping: one read of x and one write of out, so HBM bound.  A thread owns a
+// 16-byte chunk of channels (8 bf16 or 4 fp32) of one batch row and walks a run of
+// kT time steps, keeping the last K - 1 inputs in registers; a warp reads and writes
+// 512 contiguous bytes per step.  The K taps of its channels stay in registers.
+// Shapes whose rows cannot be split into aligned 16-byte chunks run one channel per
+// thread.
+#include "common.cuh"
+#include "internal.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kBlock = 128;
+constexpr int kT = 64;     // time steps per thread
+constexpr int kMaxK = 8;
+
+template <typename TIO, int VEC> struct Vec;
+template <> struct Vec<__nv_bfloat16, 8> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[8]) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(p);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, const float (&v)[8]) {
+        uint4 q;
+        uint32_t *w = &q.x;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h2);
+        }
+        *reinterpret_cast<uint4 *>(p) = q;
+    }
+};
+template <> struct Vec<float, 4> {
+    static __device__ __forceinline__ void load(const float *p, float (&v)[4]) {
+        const float4 q = *reinterpret_cast<const float4 *>(p);
+        v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    }
+    static __device__ __forceinline__ void store(float *p, const float (&v)[4]) {
+        *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+template <typename TIO> struct Vec<TIO, 1> {
+    static __device__ __forceinline__ void load(const TIO *p, float (&v)[1]) {
+        v[0] = Io<TIO>::to_f(*p);
+    }
+    static __device__ __forceinline__ void store(TIO *p, const float (&v)[1]) {
+        *p = Io<TIO>::from_f(v[0]);
+    }
+};
+
+template <typename TIO, int VEC, int K, bool kFast>
+__global__ void __launch_bounds__(kBlock) conv1d_kernel(Conv1dParams p) {
+    const TIO *__restrict__ gx = static_cast<const TIO *>(p.x);
+    const TIO *__restrict__ gprev = static_cast<const TIO *>(p.x_prev);
+    TIO *__restrict__ gout = static_cast<TIO *>(p.out);
+    const int64_t D = p.dim, L = p.seqlen;
+    const int64_t nchunk = (D + VEC - 1) / VEC;
+    const int64_t ci = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (ci >= nchunk) return;
+    const int64_t b = blockIdx.y;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.z) * kT;
+    const int64_t d0 = ci * VEC;
+
+    float w[VEC][K], bias[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+        const bool in = d0 + v < D;
+#pragma unroll
+        for (int k = 0; k < K; ++k) w[v][k] = in ? p.weight[(d0 + v) * K + k] : 0.f;
+        bias[v] = (in && p.bias) ? p.bias[d0 + v] : 0.f;
+    }
+    // window[k] holds x at t - (K - 1) + k for the step about to be computed
+    float win[K][VEC];
+#pragma unroll
+    for (int k = 0; k < K - 1; ++k) {
+        const int64_t s = t0 - (K - 1) + k;
+        float v[VEC];
+        if (s >= 0) {
+            Vec<TIO, VEC>::load(gx + (b * L + s) * D + d0, v);
+        } else if (gprev) {
+            Vec<TIO, VEC>::load(gprev + (b * (K - 1) + (K - 1 + s)) * D + d0, v);
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) v[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) win[k][e] = v[e];
+    }
+    const int64_t t1 = min(L, t0 + kT);
+    for (int64_t t = t0; t < t1; ++t) {
+        Vec<TIO, VEC>::load(gx + (b * L + t) * D + d0, win[K - 1]);
+        float out[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            float acc = bias[e];
+#pragma unroll
+            for (int k = 0; k < K; ++k) acc = fmaf(w[e][k], win[k][e], acc);
+            out[e] = p.silu ? silu<kFast>(acc) : acc;
+        }
+        Vec<TIO, VEC>::store(gout + (b * L + t) * D + d0, out);
+#pragma unroll
+        for (int k = 0; k < K - 1; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) win[k][e] = win[k + 1][e];
+    }
+}
+
+template <typename TIO, int VEC, int K>
+cudaError_t launch_k(const Conv1dParams &p, cudaStream_t stream) {
+    constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
+    const int64_t nchunk = (p.dim + VEC - 1) / VEC;
+    dim3 grid(static_cast<unsigned>((nchunk + kBlock - 1) / kBlock),
+              static_cast<unsigned>(p.batch), static_cast<unsigned>((p.seqlen + kT - 1) / kT));
+    conv1d_kernel<TIO, VEC, K, kFast><<<grid, kBlock, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename TIO, int VEC> cudaError_t launch_vec(const Conv1dParams &p, cudaStream_t st) {
+    switch (p.width) {
+        case 1: return launch_k<TIO, VEC, 1>(p, st);
+        case 2: return launch_k<TIO, VEC, 2>(p, st);
+        case 3: return launch_k<TIO, VEC, 3>(p, st);
+        case 4: return launch_k<TIO, VEC, 4>(p, st);
+        case 5: return launch_k<TIO, VEC, 5>(p, st);
+        case 6: return launch_k<TIO, VEC, 6>(p, st);
+        case 7: return launch_k<TIO, VEC, 7>(p, st);
+        case 8: return launch_k<TIO, VEC, 8>(p, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename TIO> cudaError_t launch_typed(const Conv1dParams &p, cudaStream_t stream) {
+    constexpr int kVec = 16 / sizeof(TIO);
+    const bool vec = p.dim % kVec == 0 &&
+                     reinterpret_cast<uintptr_t>(p.x) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(p.out) % 16 == 0 &&
+                     (!p.x_prev || reinterpret_cast<uintptr_t>(p.x_prev) % 16 == 0);
+    return vec ? launch_vec<TIO, kVec>(p, stream) : launch_vec<TIO, 1>(p, stream);
+}
+
+}  // namespace
+
+int conv1d_max_width() { return kMaxK; }
+
+cudaError_t launch_conv1d(const Conv1dParams &p, cudaStream_t stream) {
+    return p.io_bf16 ? launch_typed<__nv_bfloat16>(p, stream) : launch_typed<float>(p, stream);
+}
+
+}  // namespace ssm

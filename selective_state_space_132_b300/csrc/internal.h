@@ -22,6 +22,7 @@ struct ScanParams {
     float *dsum;        // (B, K, D) sum of steps of chunks 0..K-2
     void *status;       // DeviceStatus at the start of the workspace (may be null)
     int clear_status;   // the first block of this launch clears the status word
+    int zoh;            // 1: zero-order-hold input coefficient instead of dl
 };
 
 // TMA-staged scan (scan_tma.cu): warps per 32-channel block for these sizes (0 = the
@@ -43,6 +44,7 @@ struct DecodeParams {
     int64_t batch, dim, dstate;
     int io_bf16;
     int softplus;
+    int zoh;            // 1: zero-order-hold input coefficient instead of dl
     float *state;
     const void *x, *delta, *Bm, *Cm, *z;
     const float *A, *Dv, *bias;
@@ -81,5 +83,16 @@ struct SSDDecodeParams {
     void *y;
 };
 cudaError_t launch_ssd_decode(const SSDDecodeParams &p, cudaStream_t stream);
+
+struct Conv1dParams {
+    int64_t batch, seqlen, dim, width;
+    int io_bf16;
+    int silu;
+    const void *x, *x_prev;
+    const float *weight, *bias;
+    void *out;
+};
+int conv1d_max_width();
+cudaError_t launch_conv1d(const Conv1dParams &p, cudaStream_t stream);
 
 }  // namespace ssm

@@ -111,12 +111,14 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
     const int64_t t_begin = static_cast<int64_t>(c) * p.chunk_len;
     const int64_t t_end = min(L, t_begin + p.chunk_len);
 
-    float a2[NS], h[NS];
+    float a2[NS], h[NS], ia[NS];
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
         const int n = j * NS + k;
         const bool v = dval && n < N;
-        a2[k] = v ? scale_A<kFast>(p.A[d * N + n]) : 0.f;
+        const float an = v ? p.A[d * N + n] : 0.f;
+        a2[k] = scale_A<kFast>(an);
+        ia[k] = an != 0.f ? 1.f / an : 0.f;
         h[k] = (!kSummary && v && p.h0) ? p.h0[(b * D + d) * N + n] : 0.f;
     }
     if (!kSummary) {
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
                 const float dlv = v ? step_size<kFast>(Io<TIO>::to_f(rdl[r]), pbias, p.softplus)
                                     : 0.f;
                 vdl[i] = dlv;
-                vdx[i] = dlv * xv;
+                vdx[i] = p.zoh ? xv : dlv * xv;  // zoh: the coefficient multiplies x later
                 vx[i] = xv;
                 vz[i] = (v && has_z && !kSummary) ? Io<TIO>::to_f(rz[r]) : 0.f;
             }
@@ -240,7 +242,12 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
 #pragma unroll
                 for (int k = 0; k < NS; ++k) {
                     const float a = decay<kFast>(dlq[i], a2[k]);
-                    h[k] = fmaf(a, h[k], dxq[i] * bv[k]);
+                    float w = dxq[i] * bv[k];
+                    if (p.zoh) {
+                        const float vn = dlq[i] * a2[k] * (kFast ? kLn2 : 1.f);
+                        w *= zoh_coef<kFast>(dlq[i], vn, a, ia[k]);
+                    }
+                    h[k] = fmaf(a, h[k], w);
                     if (!kSummary) acc = fmaf(cv[k], h[k], acc);
                 }
                 yq[i] = acc;

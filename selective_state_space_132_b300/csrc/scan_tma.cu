@@ -149,7 +149,7 @@ template <bool kFast> __device__ __forceinline__ f2 decay2(float dl, f2 a) {
     return f2{expf(v.x), expf(v.y)};
 }
 
-template <typename TIO, int NS, int LPC, int WPC, bool kSummary>
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh>
 __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constant__ TmaMaps maps,
                                                             ScanParams p) {
     using LY = Layout<TIO, NS, LPC, WPC, kSummary>;
@@ -217,19 +217,23 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
     const int sc = lane / LPC, j = lane % LPC;
     const int64_t sd = d0 + warp * CPW + sc;
     const bool sdval = sd < D;
-    f2 a2[NS / 2], h[NS / 2];
+    f2 a2[NS / 2], h[NS / 2], ia[NS / 2];
 #pragma unroll
     for (int k = 0; k < NS / 2; ++k) {
-        float av[2], hv[2];
+        float av[2], hv[2], iv[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int n = j * NS + 2 * k + e;
-            av[e] = sdval ? scale_A<kFast>(p.A[sd * N + n]) : 0.f;
+            const float an = sdval ? p.A[sd * N + n] : 0.f;
+            av[e] = scale_A<kFast>(an);
+            iv[e] = an != 0.f ? 1.f / an : 0.f;
             hv[e] = (!kSummary && sdval && p.h0) ? p.h0[(b * D + sd) * N + n] : 0.f;
         }
         a2[k] = f2{av[0], av[1]};
         h[k] = f2{hv[0], hv[1]};
+        ia[k] = f2{iv[0], iv[1]};
     }
+    (void)ia;
     if (!kSummary) {
         // fold the summaries of the chunks before this one into the initial state
         for (int cc = 0; cc < c; ++cc) {
@@ -279,7 +283,7 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
                     const int cc = q * EC + e;
                     const float dl = tval ? step_size<kFast>(vd[e], pbias[cc], p.softplus) : 0.f;
                     *reinterpret_cast<float2 *>(dlx + (warp * CPW + cc) * LY::kDlxRow + 2 * lane) =
-                        make_float2(dl, dl * vx[e]);
+                        make_float2(dl, kZoh ? vx[e] : dl * vx[e]);
                 }
             }
             if constexpr (LY::kConvBC) {
@@ -346,7 +350,16 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
 #pragma unroll
                     for (int k = 0; k < NS / 2; ++k) {
                         av[u][k] = decay2<kFast>(dl[u], a2[k]);
-                        uv[u][k] = ptx::mul2(f2{dx[u], dx[u]}, bp[u][k]);
+                        if (kZoh) {
+                            // dx holds x here: B̄ x = ((exp(dl A) - 1) / A) B x
+                            constexpr float kToNat = kFast ? kLn2 : 1.f;
+                            const f2 v = ptx::mul2(f2{dl[u] * kToNat, dl[u] * kToNat}, a2[k]);
+                            const f2 cf{zoh_coef<kFast>(dl[u], v.x, av[u][k].x, ia[k].x),
+                                        zoh_coef<kFast>(dl[u], v.y, av[u][k].y, ia[k].y)};
+                            uv[u][k] = ptx::mul2(cf, ptx::mul2(f2{dx[u], dx[u]}, bp[u][k]));
+                        } else {
+                            uv[u][k] = ptx::mul2(f2{dx[u], dx[u]}, bp[u][k]);
+                        }
                     }
                 }
                 float acc[kU];
@@ -485,11 +498,11 @@ bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t B, int64_t L,
     return r == CUDA_SUCCESS;
 }
 
-template <typename TIO, int NS, int LPC, int WPC, bool kSummary>
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh>
 cudaError_t launch_tma_one(const ScanParams &p, const TmaMaps &maps, int nchunks_grid,
                            cudaStream_t stream) {
     using LY = Layout<TIO, NS, LPC, WPC, kSummary>;
-    auto kern = scan_tma_kernel<TIO, NS, LPC, WPC, kSummary>;
+    auto kern = scan_tma_kernel<TIO, NS, LPC, WPC, kSummary, kZoh>;
     if (LY::bytes > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              LY::bytes);
@@ -502,7 +515,7 @@ cudaError_t launch_tma_one(const ScanParams &p, const TmaMaps &maps, int nchunks
 }
 
 // Blocks of 32 channels: WPC = LPC warps of 32 / LPC channels each.
-template <typename TIO, int NS, int LPC>
+template <typename TIO, int NS, int LPC, bool kZoh>
 cudaError_t launch_tma_pair(ScanParams p, cudaStream_t stream) {
     constexpr int WPC = LPC;
     using LY = Layout<TIO, NS, LPC, WPC, false>;
@@ -518,11 +531,12 @@ cudaError_t launch_tma_pair(ScanParams p, cudaStream_t stream) {
     if (!ok) return cudaErrorInvalidValue;
     p.clear_status = 1;
     if (p.nchunks > 1) {
-        cudaError_t e = launch_tma_one<TIO, NS, LPC, WPC, true>(p, m, p.nchunks - 1, stream);
+        cudaError_t e =
+            launch_tma_one<TIO, NS, LPC, WPC, true, kZoh>(p, m, p.nchunks - 1, stream);
         if (e != cudaSuccess) return e;
         p.clear_status = 0;
     }
-    return launch_tma_one<TIO, NS, LPC, WPC, false>(p, m, p.nchunks, stream);
+    return launch_tma_one<TIO, NS, LPC, WPC, false, kZoh>(p, m, p.nchunks, stream);
 }
 
 }  // namespace
@@ -555,23 +569,27 @@ bool scan_tma_pointers_ok(const void *const *ptrs, int nptrs) {
     return encoder() != nullptr;
 }
 
-cudaError_t launch_scan_tma(const ScanParams &p, cudaStream_t stream) {
+template <bool kZoh> cudaError_t launch_scan_tma_disc(const ScanParams &p, cudaStream_t stream) {
     const int64_t N = p.dstate;
     if (p.io_bf16) {
         using T = __nv_bfloat16;
-        if (N == 8) return launch_tma_pair<T, 4, 2>(p, stream);
-        if (N == 16) return launch_tma_pair<T, 4, 4>(p, stream);
-        if (N == 32) return launch_tma_pair<T, 8, 4>(p, stream);
-        if (N == 64) return launch_tma_pair<T, 16, 4>(p, stream);
+        if (N == 8) return launch_tma_pair<T, 4, 2, kZoh>(p, stream);
+        if (N == 16) return launch_tma_pair<T, 4, 4, kZoh>(p, stream);
+        if (N == 32) return launch_tma_pair<T, 8, 4, kZoh>(p, stream);
+        if (N == 64) return launch_tma_pair<T, 16, 4, kZoh>(p, stream);
     } else {
         using T = float;
-        if (N == 4) return launch_tma_pair<T, 2, 2>(p, stream);
-        if (N == 8) return launch_tma_pair<T, 4, 2>(p, stream);
-        if (N == 16) return launch_tma_pair<T, 4, 4>(p, stream);
-        if (N == 32) return launch_tma_pair<T, 8, 4>(p, stream);
-        if (N == 64) return launch_tma_pair<T, 16, 4>(p, stream);
+        if (N == 4) return launch_tma_pair<T, 2, 2, kZoh>(p, stream);
+        if (N == 8) return launch_tma_pair<T, 4, 2, kZoh>(p, stream);
+        if (N == 16) return launch_tma_pair<T, 4, 4, kZoh>(p, stream);
+        if (N == 32) return launch_tma_pair<T, 8, 4, kZoh>(p, stream);
+        if (N == 64) return launch_tma_pair<T, 16, 4, kZoh>(p, stream);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_scan_tma(const ScanParams &p, cudaStream_t stream) {
+    return p.zoh ? launch_scan_tma_disc<true>(p, stream) : launch_scan_tma_disc<false>(p, stream);
 }
 
 }  // namespace ssm

@@ -35,6 +35,8 @@ ssm_status check_scan(const ssm_scan_args *a, bool pointers = true) {
     if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
     if (a->delta_softplus != 0 && a->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
     if (a->time_chunk < 0 || a->time_chunk % 32 != 0) return SSM_ERR_INVALID_ARG;
+    if (a->discretization != SSM_DISC_EULER && a->discretization != SSM_DISC_ZOH)
+        return SSM_ERR_INVALID_ARG;
     if (a->dstate > 64) return SSM_ERR_UNSUPPORTED;
     if (a->batch > 65535) return SSM_ERR_UNSUPPORTED;
     if (a->seqlen > (int64_t)1 << 40 || a->dim > (int64_t)1 << 31) return SSM_ERR_UNSUPPORTED;
@@ -145,6 +147,8 @@ ssm_status check_decode(const ssm_decode_args *a) {
     if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
     if (a->delta_softplus != 0 && a->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
     if (a->dstate > 64) return SSM_ERR_UNSUPPORTED;
+    if (a->discretization != SSM_DISC_EULER && a->discretization != SSM_DISC_ZOH)
+        return SSM_ERR_INVALID_ARG;
     if (a->batch * a->dim * 16 > ((int64_t)1 << 40)) return SSM_ERR_UNSUPPORTED;
     if (a->batch * a->dim > 0 &&
         (!a->state || !a->x || !a->delta || !a->B || !a->C || !a->A || !a->y))
@@ -188,6 +192,28 @@ ssm_status check_ssd_decode(const ssm_ssd_decode_args *a) {
     const size_t st = (size_t)(a->batch * a->nheads * a->headdim * a->dstate) * 4;
     if (overlaps(a->y, tok, a->x, tok) || overlaps(a->y, tok, a->z, tok) ||
         overlaps(a->y, tok, a->state, st))
+        return SSM_ERR_INVALID_ARG;
+    return SSM_OK;
+}
+
+// ------------------------------------------------------------------ conv1d
+ssm_status check_conv1d(const ssm_conv1d_args *a) {
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->batch < 0 || a->seqlen < 0 || a->dim < 0 || a->width < 1) return SSM_ERR_INVALID_ARG;
+    if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (a->silu != 0 && a->silu != 1) return SSM_ERR_INVALID_ARG;
+    if (a->width > ssm::conv1d_max_width()) return SSM_ERR_UNSUPPORTED;
+    if (a->batch > 65535 || (a->seqlen + 63) / 64 > 65535) return SSM_ERR_UNSUPPORTED;
+    const bool work = a->batch * a->seqlen * a->dim > 0;
+    if (work && (!a->x || !a->out || !a->weight)) return SSM_ERR_INVALID_ARG;
+    const size_t e = io_size(a->io_dtype);
+    const void *io_ptrs[] = {a->x, a->x_prev, a->out};
+    for (const void *p : io_ptrs)
+        if (!aligned(p, e)) return SSM_ERR_ALIGNMENT;
+    if (!aligned(a->weight, 4) || !aligned(a->bias, 4)) return SSM_ERR_ALIGNMENT;
+    const size_t tok = (size_t)(a->batch * a->seqlen * a->dim) * e;
+    const size_t prev = (size_t)(a->batch * (a->width - 1) * a->dim) * e;
+    if (overlaps(a->out, tok, a->x, tok) || overlaps(a->out, tok, a->x_prev, prev))
         return SSM_ERR_INVALID_ARG;
     return SSM_OK;
 }
@@ -270,6 +296,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_args *a, ssm_stream_t stream) {
     p.chunk_len = cl;
     p.nchunks = k;
     p.status = a->workspace;
+    p.zoh = a->discretization == SSM_DISC_ZOH;
     if (k > 1) {
         char *ws = static_cast<char *>(a->workspace) + kStatusBytes;
         const size_t rows = (size_t)a->batch * k * a->dim;
@@ -318,6 +345,7 @@ ssm_status ssm_step_decode(const ssm_decode_args *a, ssm_stream_t stream) {
     p.dstate = a->dstate;
     p.io_bf16 = a->io_dtype == SSM_BF16;
     p.softplus = a->delta_softplus;
+    p.zoh = a->discretization == SSM_DISC_ZOH;
     p.state = a->state;
     p.x = a->x;
     p.delta = a->delta;
@@ -354,6 +382,25 @@ ssm_status ssm_ssd_step_decode(const ssm_ssd_decode_args *a, ssm_stream_t stream
     p.bias = a->delta_bias;
     p.y = a->y;
     return from_cuda(ssm::launch_ssd_decode(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ssm_status ssm_conv1d(const ssm_conv1d_args *a, ssm_stream_t stream) {
+    ssm_status s = check_conv1d(a);
+    if (s != SSM_OK) return s;
+    if (a->batch * a->seqlen * a->dim == 0) return SSM_OK;
+    ssm::Conv1dParams p{};
+    p.batch = a->batch;
+    p.seqlen = a->seqlen;
+    p.dim = a->dim;
+    p.width = a->width;
+    p.io_bf16 = a->io_dtype == SSM_BF16;
+    p.silu = a->silu;
+    p.x = a->x;
+    p.x_prev = a->x_prev;
+    p.weight = a->weight;
+    p.bias = a->bias;
+    p.out = a->out;
+    return from_cuda(ssm::launch_conv1d(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ssm_status ssm_read_device_status(const void *workspace, ssm_stream_t stream,

@@ -89,7 +89,10 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(DecodeParams p) {
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
             const float da = decay<kFast>(dl, scale_A<kFast>(a[k]));
-            h[k] = fmaf(da, h[k], dx * bv[k]);
+            float w = dx * bv[k];
+            if (p.zoh)  // zero-order hold: ((exp(dl A) - 1) / A) B x
+                w = zoh_coef<kFast>(dl, dl * a[k], da, a[k] != 0.f ? 1.f / a[k] : 0.f) * xv * bv[k];
+            h[k] = fmaf(da, h[k], w);
             acc = fmaf(cv[k], h[k], acc);
         }
         if (kVec) {

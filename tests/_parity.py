@@ -32,7 +32,8 @@ def run_scan(p, time_chunk=0, h_final=True, stream=None):
     y, hf = ssm.scan_fwd(dev(p.x, io), dev(p.delta, io), dev(p.A), dev(p.B, io), dev(p.C, io),
                          D=dev(p.D), z=dev(p.z, io), delta_bias=dev(p.bias),
                          delta_softplus=p.softplus, h0=dev(p.h0), return_final_state=h_final,
-                         time_chunk=time_chunk, stream=stream)
+                         time_chunk=time_chunk, stream=stream,
+                         discretization="zoh" if p.zoh else "euler")
     torch.cuda.synchronize()
     return host(y), host(hf)
 

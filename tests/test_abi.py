@@ -35,7 +35,7 @@ def test_header_declares_expected_entry_points():
     fns = header_functions()
     for name in ("ssm_scan_fwd", "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_ssd_plan",
                  "ssm_scan_workspace_size", "ssm_ssd_workspace_size", "ssm_status_string",
-                 "ssm_version", "ssm_read_device_status"):
+                 "ssm_version", "ssm_read_device_status", "ssm_conv1d"):
         assert name in fns
 
 
@@ -78,6 +78,9 @@ def test_scan_rejects_bad_arguments(lib):
     assert _scan_rc(lib, io_dtype=7) == INVALID
     assert _scan_rc(lib, delta_softplus=2) == INVALID
     assert _scan_rc(lib, time_chunk=33) == INVALID
+    a = _scan()
+    a.discretization = 2                               # neither Euler nor ZOH
+    assert lib.ssm_scan_fwd(ctypes.byref(a), None) == INVALID
     assert _scan_rc(lib, dstate=65) == UNSUPPORTED
     assert _scan_rc(lib, batch=70000) == UNSUPPORTED
     assert _scan_rc(lib, x=None) == INVALID
@@ -199,6 +202,26 @@ def test_ssd_decode_rejects_bad_arguments(lib):
     assert rc(x=0x200001) == ALIGN
     assert rc(y=0x200000) == INVALID                 # y aliases x
     assert rc(batch=0) == OK                         # nothing to do, nothing launched
+
+
+def test_conv1d_rejects_bad_arguments(lib):
+    def rc(**kw):
+        base = dict(batch=2, seqlen=64, dim=32, width=4, io_dtype=1, silu=1, x=0x100000,
+                    x_prev=None, weight=0x200000, bias=None, out=0x300000)
+        base.update(kw)
+        a = bd.Conv1dArgs(**base)
+        return lib.ssm_conv1d(ctypes.byref(a), None)
+    assert lib.ssm_conv1d(None, None) == INVALID
+    assert rc(width=0) == INVALID
+    assert rc(width=9) == UNSUPPORTED
+    assert rc(silu=2) == INVALID
+    assert rc(io_dtype=5) == INVALID
+    assert rc(weight=None) == INVALID
+    assert rc(x=0x100001) == ALIGN
+    assert rc(weight=0x200002) == ALIGN
+    assert rc(out=0x100000) == INVALID               # out aliases x
+    assert rc(out=0x400000, x_prev=0x400010) == INVALID   # out overlaps x_prev
+    assert rc(seqlen=0) == OK                        # nothing to do, nothing launched
 
 
 def test_ops_fail_loudly_without_library(monkeypatch, tmp_path):

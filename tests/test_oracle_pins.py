@@ -449,3 +449,38 @@ def test_zoh_limits():
         yz, _ = oracle.scan(**q.oracle_args())
         diffs.append(np.abs(yz - ye).max() / np.abs(ye).max())
     assert diffs[1] < diffs[0] * 0.02   # one decade of dl -> about two decades of error
+
+
+# ---------------------------------------------------------------- causal conv1d + SiLU
+def test_conv1d_equals_numpy_convolution():
+    """The causal depthwise convolution equals numpy.convolve per channel (a textbook
+    routine; the kernel reversed, since the layer correlates), then SiLU."""
+    rng = _rng(21)
+    nb, L, D, K = 2, 17, 5, 4
+    x = rng.standard_normal((nb, L, D))
+    w = rng.standard_normal((D, K))
+    bias = rng.standard_normal(D)
+    out = oracle.conv1d(x, w, bias)
+    for b in range(nb):
+        for d in range(D):
+            pre = np.convolve(x[b, :, d], w[d, ::-1])[:L] + bias[d]
+            np.testing.assert_allclose(out[b, :, d], pre / (1 + np.exp(-pre)), rtol=1e-13,
+                                       atol=1e-13)
+
+
+def test_conv1d_impulse_and_carried_window():
+    rng = _rng(22)
+    D, K = 3, 4
+    w = rng.standard_normal((D, K))
+    # a unit impulse at t = 2 reads the kernel back, last tap first (no bias, no SiLU)
+    x = np.zeros((1, 9, D))
+    x[0, 2, :] = 1.0
+    out = oracle.conv1d(x, w, silu=False)
+    for k in range(K):
+        np.testing.assert_allclose(out[0, 2 + k], w[:, K - 1 - k], rtol=0, atol=0)
+    # splitting a sequence and carrying the last K-1 inputs equals one call
+    x = rng.standard_normal((2, 20, D))
+    full = oracle.conv1d(x, w, silu=True)
+    first = oracle.conv1d(x[:, :11], w, silu=True)
+    second = oracle.conv1d(x[:, 11:], w, x_prev=x[:, 11 - (K - 1):11], silu=True)
+    np.testing.assert_allclose(np.concatenate([first, second], 1), full, rtol=1e-14, atol=1e-14)

@@ -67,3 +67,21 @@ def test_decode_full_size_sampled_rows():
     sequences against the streaming oracle."""
     p = W.config_problem(4)
     _decode_run(p, p.steps, rows=[0, 1, 77, 128, 200, 255])
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_decode_zero_order_hold(io):
+    p = W.decode_problem(4, 40, 16, 6, io=io, seed=150)
+    io_t = io_dtype(p.io)
+    state = dev(p.state0)
+    ref = p.state0.astype(np.float64).copy()
+    A, Dv, bias = dev(p.A), dev(p.D), dev(p.bias)
+    for s in range(6):
+        tok = p.tokens(s)
+        y = ssm.step_decode(state, dev(tok["x"], io_t), dev(tok["delta"], io_t), A,
+                            dev(tok["B"], io_t), dev(tok["C"], io_t), D=Dv, z=dev(tok["z"], io_t),
+                            delta_bias=bias, discretization="zoh")
+        yr = oracle.decode_step(ref, tok["x"], tok["delta"], p.A, tok["B"], tok["C"], Dv=p.D,
+                                z=tok["z"], bias=p.bias, zoh=True)
+        assert_close(host(y), yr, p.io, f"y step {s}")
+    assert_close(host(state), ref, p.io, "state")

@@ -112,3 +112,14 @@ def test_long_context_full_size_sampled_channels():
     yr, hr = oracle.scan(**args)
     assert_close(y[:, :, sel], yr, "bf16", "y")
     assert_close(hf[:, sel], hr, "bf16", "h_final")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N,time_chunk", [(16, 0), (16, 64), (5, 0), (64, 96)])
+def test_zero_order_hold(io, N, time_chunk):
+    """B̄ = (exp(dl A) - 1) / A B (the tildalice page's zero-order hold): TMA and general
+    kernels, single pass and time split, including a channel with A = 0 (limit dl B)."""
+    p = W.scan_problem(2, 150, 40, N, io=io, seed=140 + N, h0=True, A="random")
+    p.A[3, :] = 0.0
+    p.zoh = True
+    _check(p, time_chunk=time_chunk)
