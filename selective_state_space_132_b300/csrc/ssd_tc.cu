@@ -20,7 +20,8 @@
 // tiles whose below-diagonal block goes through the state at the tile boundary,
 // which is the same sum factored through rank N.
 //
-// B300 mapping (one thread block per (b, h) chain, 128 threads = one TMEM lane each):
+// B300 mapping (persistent blocks of 256 threads: two warps per TMEM lane quadrant,
+// each thread one lane (row) and half of the columns):
 //   * TMA (128-byte swizzle) brings C, B (Q x N), X (Q x P) and z of a chunk into
 //     shared memory in the canonical UMMA layouts.
 //   * Four bf16 MMAs per chunk with fp32 accumulators in TMEM:
@@ -31,7 +32,8 @@
 //   * CUDA cores build Xw (bf16, swizzled shared memory) and M (bf16 pairs written
 //     to TMEM with tcgen05.st; pairwise exponentials on the diagonal 32 x 32 blocks,
 //     a product of two factors <= 1 below them), update the fp32 state held in
-//     registers (thread n owns row n of S^T) and finish y = Yd + exp(Lam_t) Yo + D x,
+//     registers (threads n and n + 128 own the two halves of row n of S^T) and finish
+//     y = Yd + exp(Lam_t) Yo + D x,
 //     which goes back to HBM through a TMA store.
 // Two blocks share an SM: TMEM is cut to 256 columns by writing M (bf16 pairs) over
 // the G accumulator and reading it as the A operand of the M X product straight from
@@ -56,7 +58,8 @@ using ptx::f2;
 constexpr int kQ = 128;   // chunk length (MMA M)
 constexpr int kP = 64;    // head dim
 constexpr int kN = 128;   // state size
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;   // two warps per TMEM lane quadrant
+constexpr int kPH = kP / 2;     // columns of P (or of a state row) one thread handles
 constexpr int kTmemCols = 256;  // two blocks per SM share the 512 columns
 // TMEM columns: G (fp32, 128) whose first 64 columns are then overwritten by M
 // (bf16 pairs) and whose last 64 by the chunk state Sc; Yd and Yo (fp32, 64 each).
@@ -132,6 +135,9 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    // row = TMEM lane (chunk step t, or state n) of this thread; hh = which half of the
+    // P columns it handles; q4 = its lane quadrant (warps q4 and q4 + 4 share it)
+    const int row = tid & 127, hh = tid >> 7, q4 = warp & 3;
     const int64_t H = p.nheads, L = p.seqlen;
     const __nv_bfloat16 *gdt = static_cast<const __nv_bfloat16 *>(p.delta);
     DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
@@ -156,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const int k = static_cast<int>(reinterpret_cast<volatile uint32_t *>(s_red)[0]);
     __syncthreads();  // s_red is reused for the warp totals
 
@@ -192,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
     const int nseg = (u1 > u0) ? (has_head ? 1 : 0) + static_cast<int>(nfull) + (has_tail ? 1 : 0)
                                : 0;
 
-    float S[kP];
+    float S[kPH];
     for (int seg = 0; seg < nseg && ok; ++seg) {
         // kind: 1 head (publishes), 0 whole chain, 2 tail (acquires)
         int kind;
@@ -226,14 +232,14 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
             src = p.h0 ? p.h0 + (static_cast<int64_t>(b) * H + h) * kP * kN : nullptr;
         }
 #pragma unroll
-        for (int pp = 0; pp < kP; ++pp) S[pp] = src ? __ldcg(src + pp * kN + tid) : 0.f;
+        for (int pp = 0; pp < kPH; ++pp) S[pp] = src ? __ldcg(src + (kPH * hh + pp) * kN + row) : 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) st_chunk(sW, tid, q, pack8(S + 8 * q));
+        for (int q = 0; q < 4; ++q) st_chunk(sW, row, 4 * hh + q, pack8(S + 8 * q));
         ptx::fence_proxy_async_smem();  // the first Yo MMA reads sW
 
         float raw_next = 0.f;
         {
-            const int64_t t = static_cast<int64_t>(c_lo) * kQ + tid;
+            const int64_t t = static_cast<int64_t>(c_lo) * kQ + row;
             if (t < L) raw_next = __bfloat162float(gdt[(static_cast<int64_t>(b) * L + t) * H + h]);
         }
 
@@ -261,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
             }
             // ---- (b) step sizes (the raw value was fetched one chunk ahead), the running
             //      log2-decay and the column factors of the mask
-            const int64_t t = t0 + tid;
+            const int64_t t = t0 + row;
             const float raw = raw_next;
             if (c + 1 < c_hi && t + kQ < L)
                 raw_next = __bfloat162float(gdt[(static_cast<int64_t>(b) * L + t + kQ) * H + h]);
@@ -274,15 +280,18 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
             }
             // lam of the last step of this warp's 32-step block (before adding earlier warps)
             const float lam_blk = __shfl_sync(0xffffffffu, lam, 31);
-            if (lane == 31) s_red[warp] = lam;
+            // (both halves compute the same values; the first half publishes them)
+            if (lane == 31 && hh == 0) s_red[warp] = lam;
             __syncthreads();
             float base = 0.f;
-            for (int w = 0; w < warp; ++w) base += s_red[w];
+            for (int w = 0; w < q4; ++w) base += s_red[w];
             lam += base;
-            // v_s = exp(Lam_e - Lam_s) dl_s with e the last step of the block holding s
-            s_v[tid] = ex2_approx((base + lam_blk) - lam) * dl;
-            s_dl[tid] = dl;
-            s_lam[tid] = lam;
+            if (hh == 0) {
+                // v_s = exp(Lam_e - Lam_s) dl_s with e the last step of the block holding s
+                s_v[row] = ex2_approx((base + lam_blk) - lam) * dl;
+                s_dl[row] = dl;
+                s_lam[row] = lam;
+            }
 
             if (!wait_all(bar_load, ph_load)) {
                 ok = false;
@@ -324,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
                 const float w = ex2_approx(lam_tot - lam) * dl;
                 const f2 w2{w, w};
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint4 v = ld_chunk(sX, tid, q);
+                for (int q = 4 * hh; q < 4 * hh + 4; ++q) {
+                    const uint4 v = ld_chunk(sX, row, q);
                     const uint32_t in[4] = {v.x, v.y, v.z, v.w};
                     uint32_t out[4];
 #pragma unroll
@@ -333,46 +342,56 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
                         const f2 e = ptx::mul2(ptx::bf2_to_f2(in[i]), w2);
                         out[i] = ptx::f2_to_bf2(e.x, e.y);
                     }
-                    st_chunk(sW, tid, q, make_uint4(out[0], out[1], out[2], out[3]));
+                    st_chunk(sW, row, q, make_uint4(out[0], out[1], out[2], out[3]));
                 }
             }
             // ---- (e) M[t, s] = G[t, s] exp(Lam_t - Lam_s) dl_s, s <= t, as bf16 pairs over
-            //      G's first 64 columns (row t = tid).  Blocks of 32 columns: below the
-            //      diagonal block exp(Lam_t - Lam_s) = u_t v_s / dl_s with
-            //      u_t = exp(Lam_t - Lam_e), both factors <= 1; on it, pairwise exponentials.
+            //      G's first 64 columns (row t).  Blocks of 32 columns: below the diagonal
+            //      block exp(Lam_t - Lam_s) = u_t v_s / dl_s with u_t = exp(Lam_t - Lam_e),
+            //      both factors <= 1; on it, pairwise exponentials.  This thread builds the
+            //      column blocks hh and hh + 2; M overwrites G, so every warp first reads
+            //      what it needs of G, then the block synchronises, then M is stored.
+            {
+                uint32_t packed[2][16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t packed[16];
-                if (i < warp) {
-                    float gv[32];
-                    ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
-                    const float u = ex2_approx(lam - s_lam[32 * i + 31]);
+                for (int r = 0; r < 2; ++r) {
+                    const int i = hh + 2 * r;
+                    if (i < q4) {
+                        float gv[32];
+                        ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
+                        const float u = ex2_approx(lam - s_lam[32 * i + 31]);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 vv = *reinterpret_cast<const float2 *>(s_v + 32 * i + 2 * e);
-                        const f2 m = ptx::mul2(ptx::mul2(f2{gv[2 * e], gv[2 * e + 1]}, f2{u, u}),
-                                               f2{vv.x, vv.y});
-                        packed[e] = ptx::f2_to_bf2(m.x, m.y);
-                    }
-                } else if (i == warp) {
-                    float gv[32];
-                    ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float m2[2];
-#pragma unroll
-                        for (int u2 = 0; u2 < 2; ++u2) {
-                            const int s = 32 * i + 2 * e + u2;
-                            const float val = gv[2 * e + u2] * ex2_approx(lam - s_lam[s]) * s_dl[s];
-                            m2[u2] = s <= tid ? val : 0.f;
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 vv = *reinterpret_cast<const float2 *>(s_v + 32 * i + 2 * e);
+                            const f2 m = ptx::mul2(ptx::mul2(f2{gv[2 * e], gv[2 * e + 1]}, f2{u, u}),
+                                                   f2{vv.x, vv.y});
+                            packed[r][e] = ptx::f2_to_bf2(m.x, m.y);
                         }
-                        packed[e] = ptx::f2_to_bf2(m2[0], m2[1]);
-                    }
-                } else {
+                    } else if (i == q4) {
+                        float gv[32];
+                        ptx::tmem_ld32(tmem + lane_base + kColG + 32 * i, gv);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) packed[e] = 0u;
+                        for (int e = 0; e < 16; ++e) {
+                            float m2[2];
+#pragma unroll
+                            for (int u2 = 0; u2 < 2; ++u2) {
+                                const int sc = 32 * i + 2 * e + u2;
+                                const float val = gv[2 * e + u2] * ex2_approx(lam - s_lam[sc]) * s_dl[sc];
+                                m2[u2] = sc <= row ? val : 0.f;
+                            }
+                            packed[r][e] = ptx::f2_to_bf2(m2[0], m2[1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) packed[r][e] = 0u;
+                    }
                 }
-                ptx::tmem_st16(tmem + lane_base + kColM + 16 * i, packed);
+                ptx::tc_fence_before();
+                __syncthreads();  // every read of G is done
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+                    ptx::tmem_st16(tmem + lane_base + kColM + 16 * (hh + 2 * r), packed[r]);
             }
             ptx::tmem_wait_st();
             ptx::fence_proxy_async_smem();
@@ -401,36 +420,33 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
             }
             ph_mma ^= 1;
             ptx::tc_fence_after();
-            // ---- (g) state: S <- exp(Lam_end) S + Sc (row n = tid), bf16 copy into sW
+            // ---- (g) state: S <- exp(Lam_end) S + Sc (row n, columns of this half), bf16
+            //      copy into sW
             {
                 const float dec = ex2_approx(lam_tot);
+                float sc[32];
+                ptx::tmem_ld32(tmem + lane_base + kColSc + kPH * hh, sc);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float sc[32];
-                    ptx::tmem_ld32(tmem + lane_base + kColSc + 32 * half, sc);
+                for (int pp = 0; pp < kPH; ++pp) S[pp] = fmaf(dec, S[pp], sc[pp]);
 #pragma unroll
-                    for (int pp = 0; pp < 32; ++pp)
-                        S[32 * half + pp] = fmaf(dec, S[32 * half + pp], sc[pp]);
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q) st_chunk(sW, tid, q, pack8(S + 8 * q));
+                for (int q = 0; q < 4; ++q) st_chunk(sW, row, 4 * hh + q, pack8(S + 8 * q));
             }
             // ---- (h) y = Yd + exp(Lam_t) Yo + D x (x gate), written over X in place
             {
                 const float et = ex2_approx(lam);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                {
+                    const int half = hh;
                     float yd[32], yo[32];
                     ptx::tmem_ld32(tmem + lane_base + kColYd + 32 * half, yd);
                     ptx::tmem_ld32(tmem + lane_base + kColYo + 32 * half, yo);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int qq = half * 4 + q;
-                        const uint4 xv = ld_chunk(sX, tid, qq);
+                        const uint4 xv = ld_chunk(sX, row, qq);
                         const uint32_t xin[4] = {xv.x, xv.y, xv.z, xv.w};
                         uint32_t zin[4] = {0, 0, 0, 0};
                         if (kGate) {
-                            const uint4 zv = ld_chunk(sZ, tid, qq);
+                            const uint4 zv = ld_chunk(sZ, row, qq);
                             zin[0] = zv.x; zin[1] = zv.y; zin[2] = zv.z; zin[3] = zv.w;
                         }
                         uint32_t out[4];
@@ -448,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
                             }
                             out[e] = ptx::f2_to_bf2(y.x, y.y);
                         }
-                        st_chunk(sX, tid, qq, make_uint4(out[0], out[1], out[2], out[3]));
+                        st_chunk(sX, row, qq, make_uint4(out[0], out[1], out[2], out[3]));
                     }
                 }
             }
@@ -466,14 +482,14 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         if (kind == 1) {
             float *dst = sk.states + static_cast<int64_t>(k) * kP * kN;
 #pragma unroll
-            for (int pp = 0; pp < kP; ++pp) __stcg(dst + pp * kN + tid, S[pp]);
+            for (int pp = 0; pp < kPH; ++pp) __stcg(dst + (kPH * hh + pp) * kN + row, S[pp]);
             __threadfence();
             __syncthreads();
             if (tid == 0) ptx::st_release_u32(sk.flags + k, 1u);
         } else if (p.h_final) {
             float *hf = p.h_final + (static_cast<int64_t>(b) * H + h) * kP * kN;
 #pragma unroll
-            for (int pp = 0; pp < kP; ++pp) hf[pp * kN + tid] = S[pp];
+            for (int pp = 0; pp < kPH; ++pp) hf[(kPH * hh + pp) * kN + row] = S[pp];
         }
     }
 
