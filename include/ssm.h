@@ -113,6 +113,51 @@ SSM_API ssm_status ssm_scan_plan(const ssm_scan_args *args, int64_t *chunk_len,
                                  int32_t *nchunks, int32_t *launches);
 SSM_API ssm_status ssm_scan_fwd(const ssm_scan_args *args, ssm_stream_t stream);
 
+/* ------------------------------------------------------------------ scan backward
+ * Gradients of ssm_scan_fwd, rebuilding the hidden states from the inputs instead of
+ * storing them in the forward pass (tildalice review, section "Hardware-Aware 병렬
+ * 알고리즘", item "역전파 시 재계산"; yongggg review, section "하드웨어 인식 알고리즘").  The arithmetic is the adjoint of the recurrence of
+ * ssm_scan_fwd, with lam = dLoss/dh_t walking back in time:
+ *   g = dy silu(z);  dz = dy (C.h + D x) silu'(z);  dC_t += g h_t;  lam += g C_t;
+ *   dB_t += lam c x;  dx = g D + sum_n lam c B;  ddl = sum_n lam (h_{t-1} a A + B x dc/ddl);
+ *   dA += lam (h_{t-1} a dl + B x dc/dA);  lam *= a;  ddelta = ddl softplus'(delta + bias)
+ * with a = exp(dl A) and c = dl (Euler) or (exp(dl A) - 1)/A (zero-order hold).
+ *   - Forward inputs, sizes and flags: as in ssm_scan_args (x, delta, B, C, z in
+ *     io_dtype; A (D,N), D, delta_bias (D), h0 (B,D,N) fp32; D, delta_bias, z, h0
+ *     nullable).
+ *   - dy (B,L,D) io_dtype: gradient of y.  dh_final (B,D,N) fp32: gradient of the
+ *     final state, nullable (zero).
+ *   - Outputs, all written (never accumulated into):
+ *       dx, ddelta (B,L,D) io_dtype (ddelta is the gradient of the raw delta);
+ *       dz (B,L,D) io_dtype, required iff z is given;
+ *       dB, dC (B,L,N) fp32 (sums over channels); dA (D,N) fp32 (sum over batch rows);
+ *       dD, ddelta_bias (D) fp32, nullable (gradients of D and of the bias, computed
+ *       even when D or delta_bias is NULL, i.e. taken at zero); dh0 (B,D,N) fp32,
+ *       nullable.
+ *   - No output may overlap an input or another output.
+ *   - workspace: ssm_scan_bwd_workspace_size bytes, 256-byte aligned: a status
+ *     word and the state at the start of every time tile of every (b, d) chain, fp32.
+ *   - N <= 64; the channels of one batch row run as one chain per channel, so a
+ *     single very long sequence has B * ceil(D / 32) blocks of parallelism. */
+typedef struct {
+    int64_t batch, seqlen, dim, dstate;
+    int32_t io_dtype;
+    int32_t delta_softplus;
+    int32_t discretization;
+    int32_t reserved;
+    const void *x, *delta, *B, *C, *z;
+    const float *A, *D, *delta_bias, *h0;
+    const void *dy;
+    const float *dh_final;
+    void *dx, *ddelta, *dz;
+    float *dA, *dB, *dC, *dD, *ddelta_bias, *dh0;
+    void *workspace;
+    size_t workspace_bytes;
+} ssm_scan_bwd_args;
+
+SSM_API ssm_status ssm_scan_bwd_workspace_size(const ssm_scan_bwd_args *args, size_t *bytes);
+SSM_API ssm_status ssm_scan_bwd(const ssm_scan_bwd_args *args, ssm_stream_t stream);
+
 /* ------------------------------------------------------------------ scan without allocation
  * No counterpart in the pages: a library convenience.  Same computation, arguments
  * and results as ssm_scan_fwd, but the scratch that a time-split sequence needs

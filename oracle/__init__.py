@@ -59,6 +59,9 @@ def _load():
     lib.oracle_ssd_decode_f64.argtypes = [i64] * 5 + [dp] * 9 + [ctypes.c_int, dp, ctypes.c_int]
     lib.oracle_conv1d_f64.restype = ctypes.c_int
     lib.oracle_conv1d_f64.argtypes = [i64] * 4 + [dp] * 4 + [ctypes.c_int, dp, ctypes.c_int]
+    lib.oracle_scan_bwd_f64.restype = ctypes.c_int
+    lib.oracle_scan_bwd_f64.argtypes = ([i64] * 4 + [dp] * 8 + [ctypes.c_int, ctypes.c_int]
+                                        + [dp] * 12 + [ctypes.c_int])
     lib.oracle_softplus_f64.restype = ctypes.c_double
     lib.oracle_softplus_f64.argtypes = [ctypes.c_double]
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -106,6 +109,33 @@ def scan(x, delta, A, Bm, Cm, Dv=None, z=None, bias=None, softplus: bool = True,
     if rc != 0:
         raise RuntimeError(f"oracle_scan_f64 failed: {rc}")
     return y, hf
+
+
+def scan_bwd(gy, x, delta, A, Bm, Cm, Dv=None, z=None, bias=None, softplus: bool = True,
+             h0=None, gh_final=None, zoh: bool = False, threads: Optional[int] = None):
+    """Gradients of scan() for the upstream gradient gy (B,L,D) (and gh_final (B,D,N)
+    of the final state, zero when None).  Returns a dict with gx, gdelta (B,L,D);
+    gA (D,N); gB, gC (B,L,N); gD, gbias (D,); gz (B,L,D) when z is given; gh0 (B,D,N)."""
+    lib = _load()
+    x, delta, A, Bm, Cm = (_f64(a) for a in (x, delta, A, Bm, Cm))
+    Dv, z, bias, h0, gy, gh_final = (_f64(a) for a in (Dv, z, bias, h0, gy, gh_final))
+    nb, L, D = x.shape
+    N = A.shape[1]
+    out = dict(gx=np.empty((nb, L, D)), gdelta=np.empty((nb, L, D)), gA=np.empty((D, N)),
+               gB=np.empty((nb, L, N)), gC=np.empty((nb, L, N)), gD=np.empty(D),
+               gbias=np.empty(D), gh0=np.empty((nb, D, N)))
+    if z is not None:
+        out["gz"] = np.empty((nb, L, D))
+    rc = lib.oracle_scan_bwd_f64(nb, L, D, N, _ptr(x), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm),
+                                 _ptr(Dv), _ptr(z), _ptr(bias), int(bool(softplus)),
+                                 int(bool(zoh)), _ptr(h0), _ptr(gy), _ptr(gh_final),
+                                 _ptr(out["gx"]), _ptr(out["gdelta"]), _ptr(out["gA"]),
+                                 _ptr(out["gB"]), _ptr(out["gC"]), _ptr(out["gD"]),
+                                 _ptr(out.get("gz")), _ptr(out["gbias"]), _ptr(out["gh0"]),
+                                 threads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_scan_bwd_f64 failed: {rc}")
+    return out
 
 
 def ssd(x, delta, A, Bm, Cm, Dv=None, z=None, bias=None, softplus: bool = True,

@@ -113,6 +113,152 @@ int oracle_scan_f64(int64_t nb, int64_t L, int64_t D, int64_t N,
     return failed ? -2 : 0;
 }
 
+/* Derivatives of the ZOH input coefficient c(dl, a) = (exp(dl a) - 1) / a:
+ *   dc/d(dl) = exp(dl a)
+ *   dc/da    = dl^2 (v e^v - e^v + 1) / v^2 with v = dl a, whose power series is
+ *              dl^2 sum_{j>=0} (j+1) v^j / (j+2)!  (used for |v| < 1e-2, where the closed
+ *              form cancels; six terms leave an error below 2e-16 relative). */
+static double zoh_dc_da(double dl, double a)
+{
+    double v = dl * a;
+    if (fabs(v) < 1e-2) {
+        double s = 0.0, f = 1.0, pw = 1.0;      /* f = (j+2)! */
+        for (int j = 0; j < 6; ++j) {
+            f *= (double)(j + 2);
+            s += (double)(j + 1) * pw / f;
+            pw *= v;
+        }
+        return dl * dl * s;
+    }
+    return (dl * exp(v) - expm1(v) / a) / a;
+}
+
+static double sigmoid_f64(double v)
+{
+    return 1.0 / (1.0 + exp(-v));
+}
+
+/*
+ * Gradients of the scan above (reverse-mode, the adjoint of the recurrence).  The
+ * pages ask for the backward pass of the selective scan to rebuild the states instead
+ * of storing them (tildalice review, section "Hardware-Aware 병렬 알고리즘", item
+ * "역전파 시 재계산"; yongggg review, section "하드웨어 인식 알고리즘"); the
+ * oracle has no memory limit and keeps every h_t of one (b, d) chain, then walks
+ * back in time:
+ *   lam      = dLoss/dh_t, starting from gh_final (or 0)
+ *   g_yr     = gy_t silu(z_t)                 (gradient of C.h + D x)
+ *   gz_t     = gy_t (C.h_t + D x_t) silu'(z_t), silu'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *   gC_t,n  += g_yr h_t,n       gD += g_yr x_t       gx_t = g_yr D
+ *   lam_n   += g_yr C_t,n
+ *   with h_t,n = a h_{t-1},n + c B_t,n x_t,  a = exp(dl A_n),  c = dl (Euler) or
+ *   (exp(dl A_n) - 1)/A_n (ZOH):
+ *   gB_t,n  += lam_n c x_t      gx_t += lam_n c B_t,n
+ *   gdl_t   += lam_n (h_{t-1},n a A_n + B_t,n x_t dc/d(dl))
+ *   gA_n    += lam_n (h_{t-1},n a dl + B_t,n x_t dc/dA)
+ *   lam_n    = lam_n a            (now dLoss/dh_{t-1})
+ *   gdelta_t = gdl_t softplus'(v) = gdl_t sigmoid(v), v = delta_t + bias (or gdl_t
+ *              without softplus);  gbias += gdelta_t;  gh0 = lam at t = -1.
+ * gB, gC are summed over d; gA, gD, gbias over b (and t).  Outputs gz, gD, gbias, gh0
+ * are nullable.  gh_final (B,D,N) is nullable (zero).
+ */
+int oracle_scan_bwd_f64(int64_t nb, int64_t L, int64_t D, int64_t N,
+                        const double *x, const double *delta, const double *A,
+                        const double *Bm, const double *Cm, const double *Dv,
+                        const double *z, const double *bias, int softplus, int zoh,
+                        const double *h0, const double *gy, const double *gh_final,
+                        double *gx, double *gdelta, double *gA, double *gB, double *gC,
+                        double *gD, double *gz, double *gbias, double *gh0, int nthreads)
+{
+    if (nb < 0 || L < 0 || D < 0 || N < 1) return -1;
+    if (nthreads < 1) nthreads = 1;
+    memset(gA, 0, (size_t)(D * N) * sizeof(double));
+    memset(gB, 0, (size_t)(nb * L * N) * sizeof(double));
+    memset(gC, 0, (size_t)(nb * L * N) * sizeof(double));
+    if (gD) memset(gD, 0, (size_t)D * sizeof(double));
+    if (gbias) memset(gbias, 0, (size_t)D * sizeof(double));
+    int failed = 0;
+    for (int64_t b = 0; b < nb; ++b) {
+        /* channels of one batch row in parallel; gB/gC of this row are summed over d
+         * from per-thread copies, in channel order within a thread */
+#pragma omp parallel num_threads(nthreads) reduction(| : failed)
+        {
+            double *hs = (double *)malloc((size_t)((L + 1) * N) * sizeof(double));
+            double *lam = (double *)malloc((size_t)N * sizeof(double));
+            double *pB = (double *)calloc((size_t)(L * N), sizeof(double));
+            double *pC = (double *)calloc((size_t)(L * N), sizeof(double));
+            int ok = hs && lam && pB && pC;
+            if (!ok) failed |= 1;
+#pragma omp for schedule(static)
+            for (int64_t d = 0; d < D; ++d) {
+                if (!ok) continue;
+                const double *Ad = A + d * N;
+                double Dd = Dv ? Dv[d] : 0.0;
+                /* forward, keeping h_{-1} .. h_{L-1} in hs[0 .. L] */
+                for (int64_t n = 0; n < N; ++n) hs[n] = h0 ? h0[(b * D + d) * N + n] : 0.0;
+                for (int64_t t = 0; t < L; ++t) {
+                    int64_t bt = b * L + t;
+                    double xv = x[bt * D + d];
+                    double dl = step_size(delta[bt * D + d], bias, d, softplus);
+                    for (int64_t n = 0; n < N; ++n)
+                        hs[(t + 1) * N + n] = exp(dl * Ad[n]) * hs[t * N + n] +
+                                              input_coef(dl, Ad[n], zoh) * Bm[bt * N + n] * xv;
+                }
+                /* backward */
+                for (int64_t n = 0; n < N; ++n)
+                    lam[n] = gh_final ? gh_final[(b * D + d) * N + n] : 0.0;
+                double gD_acc = 0.0, gbias_acc = 0.0;
+                for (int64_t t = L - 1; t >= 0; --t) {
+                    int64_t bt = b * L + t;
+                    double xv = x[bt * D + d];
+                    double v = delta[bt * D + d] + (bias ? bias[d] : 0.0);
+                    double dl = softplus ? softplus_f64(v) : v;
+                    const double *ht = hs + (t + 1) * N, *hp = hs + t * N;
+                    double g_yr = gy[bt * D + d];
+                    if (z) {
+                        double zv = z[bt * D + d], sg = sigmoid_f64(zv);
+                        double yr = Dd * xv;
+                        for (int64_t n = 0; n < N; ++n) yr += Cm[bt * N + n] * ht[n];
+                        if (gz) gz[bt * D + d] = g_yr * yr * sg * (1.0 + zv * (1.0 - sg));
+                        g_yr *= zv * sg;
+                    }
+                    double gxv = g_yr * Dd, gdl = 0.0;
+                    gD_acc += g_yr * xv;
+                    for (int64_t n = 0; n < N; ++n) {
+                        double an = Ad[n], a = exp(dl * an), c = input_coef(dl, an, zoh);
+                        double Bn = Bm[bt * N + n];
+                        pC[t * N + n] += g_yr * ht[n];
+                        lam[n] += g_yr * Cm[bt * N + n];
+                        pB[t * N + n] += lam[n] * c * xv;
+                        gxv += lam[n] * c * Bn;
+                        double dc_ddl = zoh ? a : 1.0;
+                        double dc_da = zoh ? (an == 0.0 ? 0.5 * dl * dl : zoh_dc_da(dl, an)) : 0.0;
+                        gdl += lam[n] * (hp[n] * a * an + Bn * xv * dc_ddl);
+                        gA[d * N + n] += lam[n] * (hp[n] * a * dl + Bn * xv * dc_da);
+                        lam[n] *= a;
+                    }
+                    double gv = softplus ? gdl * sigmoid_f64(v) : gdl;
+                    gx[bt * D + d] = gxv;
+                    gdelta[bt * D + d] = gv;
+                    gbias_acc += gv;
+                }
+                if (gD) gD[d] += gD_acc;
+                if (gbias) gbias[d] += gbias_acc;
+                if (gh0)
+                    for (int64_t n = 0; n < N; ++n) gh0[(b * D + d) * N + n] = lam[n];
+            }
+#pragma omp critical
+            if (ok) {
+                for (int64_t i = 0; i < L * N; ++i) {
+                    gB[b * L * N + i] += pB[i];
+                    gC[b * L * N + i] += pC[i];
+                }
+            }
+            free(hs); free(lam); free(pB); free(pC);
+        }
+    }
+    return failed ? -2 : 0;
+}
+
 int oracle_ssd_f64(int64_t nb, int64_t L, int64_t H, int64_t P, int64_t G, int64_t N,
                    const double *x, const double *delta, const double *A,
                    const double *Bm, const double *Cm, const double *Dv,

@@ -17,6 +17,7 @@ _STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED",
            6: "SSM_ERR_TIMEOUT"}
 
 EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
+            "ssm_scan_bwd_workspace_size", "ssm_scan_bwd",
             "ssm_ssd_workspace_size", "ssm_ssd_chunk_fwd", "ssm_ssd_plan", "ssm_step_decode",
             "ssm_ssd_step_decode", "ssm_conv1d", "ssm_status_string", "ssm_version",
             "ssm_check_bounded_wait",
@@ -51,6 +52,16 @@ class DecodeArgs(ctypes.Structure):
                 ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp), ("z", _vp),
                 ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("y", _vp),
                 ("discretization", _i32), ("reserved", _i32)]
+
+
+class ScanBwdArgs(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("seqlen", _i64), ("dim", _i64), ("dstate", _i64),
+                ("io_dtype", _i32), ("delta_softplus", _i32), ("discretization", _i32),
+                ("reserved", _i32), ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp),
+                ("z", _vp), ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("h0", _fp),
+                ("dy", _vp), ("dh_final", _fp), ("dx", _vp), ("ddelta", _vp), ("dz", _vp),
+                ("dA", _fp), ("dB", _fp), ("dC", _fp), ("dD", _fp), ("ddelta_bias", _fp),
+                ("dh0", _fp), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class Conv1dArgs(ctypes.Structure):
@@ -117,6 +128,11 @@ def load_library():
     lib.ssm_step_decode.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
     lib.ssm_ssd_step_decode.argtypes = [ctypes.POINTER(SSDDecodeArgs), _vp]
     lib.ssm_ssd_step_decode.restype = ctypes.c_int
+    lib.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(ScanBwdArgs),
+                                                ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_int
+    lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanBwdArgs), _vp]
+    lib.ssm_scan_bwd.restype = ctypes.c_int
     lib.ssm_conv1d.argtypes = [ctypes.POINTER(Conv1dArgs), _vp]
     lib.ssm_conv1d.restype = ctypes.c_int
     lib.ssm_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
@@ -266,6 +282,57 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
     args.workspace, args.workspace_bytes = _ptr(ws), nbytes
     _raise(lib.ssm_scan_fwd(ctypes.byref(args), _stream(stream)), "ssm_scan_fwd")
     return y, h_final
+
+
+def scan_bwd(dy: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor,
+             B: torch.Tensor, C: torch.Tensor, D: Optional[torch.Tensor] = None,
+             z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
+             delta_softplus: bool = True, h0: Optional[torch.Tensor] = None,
+             dh_final: Optional[torch.Tensor] = None, discretization: str = "euler",
+             workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Gradients of scan_fwd with the same inputs, for the gradient dy (B, L, D) of y and
+    dh_final (B, D, N) fp32 of the final state (zero when None).  The hidden states
+    are recomputed, not stored.  Returns a dict: dx, ddelta (B, L, D) in x's dtype;
+    dz (when z is given); dA (D, N), dB, dC (B, L, N), dD, ddelta_bias (D,), dh0
+    (B, D, N), all fp32."""
+    lib = load_library()
+    nb, L, Dm = x.shape
+    N = A.shape[1]
+    dev, io = x.device, x.dtype
+    _scan_args(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, None, None, 0,
+               discretization)                                  # shape and dtype checks
+    _check(dy, "dy", (nb, L, Dm), io, dev)
+    _check(dh_final, "dh_final", (nb, Dm, N), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(dx=torch.empty_like(x), ddelta=torch.empty_like(x),
+             dz=torch.empty_like(x) if z is not None else None,
+             dA=torch.empty((Dm, N), **f32), dB=torch.empty((nb, L, N), **f32),
+             dC=torch.empty((nb, L, N), **f32), dD=torch.empty((Dm,), **f32),
+             ddelta_bias=torch.empty((Dm,), **f32), dh0=torch.empty((nb, Dm, N), **f32))
+    args = ScanBwdArgs(nb, L, Dm, N, _io_code(x), int(bool(delta_softplus)), _disc(discretization),
+                       0, _ptr(x), _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
+                       _ptr(delta_bias), _ptr(h0), _ptr(dy), _ptr(dh_final), _ptr(g["dx"]),
+                       _ptr(g["ddelta"]), _ptr(g["dz"]), _ptr(g["dA"]), _ptr(g["dB"]),
+                       _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
+                       None, 0)
+    need = ctypes.c_size_t(0)
+    _raise(lib.ssm_scan_bwd_workspace_size(ctypes.byref(args), ctypes.byref(need)),
+           "ssm_scan_bwd_workspace_size")
+    ws, nbytes = _workspace(int(need.value), dev, workspace)
+    args.workspace, args.workspace_bytes = _ptr(ws), nbytes
+    _raise(lib.ssm_scan_bwd(ctypes.byref(args), _stream(stream)), "ssm_scan_bwd")
+    if z is None:
+        del g["dz"]
+    return g
+
+
+def scan_bwd_workspace_size(batch: int, seqlen: int, dim: int, dstate: int,
+                            io_dtype=torch.bfloat16) -> int:
+    args = ScanBwdArgs(batch, seqlen, dim, dstate, 1 if io_dtype == torch.bfloat16 else 0, 1, 0, 0)
+    out = ctypes.c_size_t(0)
+    _raise(load_library().ssm_scan_bwd_workspace_size(ctypes.byref(args), ctypes.byref(out)),
+           "ssm_scan_bwd_workspace_size")
+    return int(out.value)
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

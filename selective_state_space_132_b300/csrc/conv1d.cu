@@ -7,8 +7,9 @@
 //
 // B300 mapping: one read of x and one write of out, so HBM bound.  A thread owns a
 // 16-byte chunk of channels (8 bf16 or 4 fp32) of one batch row and walks a run of
-// kT time steps, keeping the last K - 1 inputs in registers; a warp reads and writes
-// 512 contiguous bytes per step.  The K taps of its channels stay in registers.
+// kT time steps, keeping the last K - 1 inputs in registers and eight rows of loads in
+// flight; a warp reads and writes 512 contiguous bytes per row.  The K taps of its
+// channels stay in registers.
 // Shapes whose rows cannot be split into aligned 16-byte chunks run one channel per
 // thread.
 #include "common.cuh"
@@ -18,13 +19,18 @@ namespace ssm {
 namespace {
 
 constexpr int kBlock = 128;
-constexpr int kT = 64;     // time steps per thread
+constexpr int kT = 32;     // time steps per thread
+constexpr int kR = 8;      // rows loaded ahead (in flight per thread)
 constexpr int kMaxK = 8;
 
+// Raw 16-byte (or one-element) rows and their widening to fp32.
 template <typename TIO, int VEC> struct Vec;
 template <> struct Vec<__nv_bfloat16, 8> {
-    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[8]) {
-        const uint4 q = *reinterpret_cast<const uint4 *>(p);
+    using Raw = uint4;
+    static __device__ __forceinline__ Raw load(const __nv_bfloat16 *p) {
+        return __ldg(reinterpret_cast<const uint4 *>(p));
+    }
+    static __device__ __forceinline__ void widen(const Raw &q, float (&v)[8]) {
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -44,8 +50,11 @@ template <> struct Vec<__nv_bfloat16, 8> {
     }
 };
 template <> struct Vec<float, 4> {
-    static __device__ __forceinline__ void load(const float *p, float (&v)[4]) {
-        const float4 q = *reinterpret_cast<const float4 *>(p);
+    using Raw = float4;
+    static __device__ __forceinline__ Raw load(const float *p) {
+        return __ldg(reinterpret_cast<const float4 *>(p));
+    }
+    static __device__ __forceinline__ void widen(const Raw &q, float (&v)[4]) {
         v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
     }
     static __device__ __forceinline__ void store(float *p, const float (&v)[4]) {
@@ -53,25 +62,33 @@ template <> struct Vec<float, 4> {
     }
 };
 template <typename TIO> struct Vec<TIO, 1> {
-    static __device__ __forceinline__ void load(const TIO *p, float (&v)[1]) {
-        v[0] = Io<TIO>::to_f(*p);
+    using Raw = TIO;
+    static __device__ __forceinline__ Raw load(const TIO *p) { return *p; }
+    static __device__ __forceinline__ void widen(const Raw &q, float (&v)[1]) {
+        v[0] = Io<TIO>::to_f(q);
     }
     static __device__ __forceinline__ void store(TIO *p, const float (&v)[1]) {
         *p = Io<TIO>::from_f(v[0]);
     }
 };
 
+// One thread: VEC channels of one batch row over kT steps.  Consecutive threads take
+// consecutive channel chunks, so a warp's loads and stores cover contiguous bytes.
 template <typename TIO, int VEC, int K, bool kFast>
 __global__ void __launch_bounds__(kBlock) conv1d_kernel(Conv1dParams p) {
+    using V = Vec<TIO, VEC>;
     const TIO *__restrict__ gx = static_cast<const TIO *>(p.x);
     const TIO *__restrict__ gprev = static_cast<const TIO *>(p.x_prev);
     TIO *__restrict__ gout = static_cast<TIO *>(p.out);
     const int64_t D = p.dim, L = p.seqlen;
     const int64_t nchunk = (D + VEC - 1) / VEC;
-    const int64_t ci = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
-    if (ci >= nchunk) return;
-    const int64_t b = blockIdx.y;
-    const int64_t t0 = static_cast<int64_t>(blockIdx.z) * kT;
+    const int64_t ntb = (L + kT - 1) / kT;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (item >= p.batch * ntb * nchunk) return;
+    const int64_t ci = item % nchunk;
+    const int64_t tb = (item / nchunk) % ntb;
+    const int64_t b = item / (nchunk * ntb);
+    const int64_t t0 = tb * kT;
     const int64_t d0 = ci * VEC;
 
     float w[VEC][K], bias[VEC];
@@ -82,52 +99,57 @@ __global__ void __launch_bounds__(kBlock) conv1d_kernel(Conv1dParams p) {
         for (int k = 0; k < K; ++k) w[v][k] = in ? p.weight[(d0 + v) * K + k] : 0.f;
         bias[v] = (in && p.bias) ? p.bias[d0 + v] : 0.f;
     }
-    // window[k] holds x at t - (K - 1) + k for the step about to be computed
+    // win[k] holds x at t - (K - 1) + k for the step about to be computed
     float win[K][VEC];
 #pragma unroll
     for (int k = 0; k < K - 1; ++k) {
         const int64_t s = t0 - (K - 1) + k;
-        float v[VEC];
         if (s >= 0) {
-            Vec<TIO, VEC>::load(gx + (b * L + s) * D + d0, v);
+            V::widen(V::load(gx + (b * L + s) * D + d0), win[k]);
         } else if (gprev) {
-            Vec<TIO, VEC>::load(gprev + (b * (K - 1) + (K - 1 + s)) * D + d0, v);
+            V::widen(V::load(gprev + (b * (K - 1) + (K - 1 + s)) * D + d0), win[k]);
         } else {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) v[e] = 0.f;
+            for (int e = 0; e < VEC; ++e) win[k][e] = 0.f;
         }
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) win[k][e] = v[e];
     }
     const int64_t t1 = min(L, t0 + kT);
-    for (int64_t t = t0; t < t1; ++t) {
-        Vec<TIO, VEC>::load(gx + (b * L + t) * D + d0, win[K - 1]);
-        float out[VEC];
+    for (int64_t ta = t0; ta < t1; ta += kR) {
+        typename V::Raw raw[kR];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            float acc = bias[e];
+        for (int r = 0; r < kR; ++r)
+            if (ta + r < t1) raw[r] = V::load(gx + (b * L + ta + r) * D + d0);
 #pragma unroll
-            for (int k = 0; k < K; ++k) acc = fmaf(w[e][k], win[k][e], acc);
-            out[e] = p.silu ? silu<kFast>(acc) : acc;
+        for (int r = 0; r < kR; ++r) {
+            if (ta + r < t1) {
+                V::widen(raw[r], win[K - 1]);
+                float out[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    float acc = bias[e];
+#pragma unroll
+                    for (int k = 0; k < K; ++k) acc = fmaf(w[e][k], win[k][e], acc);
+                    out[e] = p.silu ? silu<kFast>(acc) : acc;
+                }
+                V::store(gout + (b * L + ta + r) * D + d0, out);
+#pragma unroll
+                for (int k = 0; k < K - 1; ++k)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) win[k][e] = win[k + 1][e];
+            }
         }
-        Vec<TIO, VEC>::store(gout + (b * L + t) * D + d0, out);
-#pragma unroll
-        for (int k = 0; k < K - 1; ++k)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) win[k][e] = win[k + 1][e];
     }
 }
 
 template <typename TIO, int VEC, int K>
 cudaError_t launch_k(const Conv1dParams &p, cudaStream_t stream) {
     constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
-    const int64_t nchunk = (p.dim + VEC - 1) / VEC;
-    dim3 grid(static_cast<unsigned>((nchunk + kBlock - 1) / kBlock),
-              static_cast<unsigned>(p.batch), static_cast<unsigned>((p.seqlen + kT - 1) / kT));
-    conv1d_kernel<TIO, VEC, K, kFast><<<grid, kBlock, 0, stream>>>(p);
+    const int64_t items = p.batch * ((p.seqlen + kT - 1) / kT) * ((p.dim + VEC - 1) / VEC);
+    const int64_t blocks = (items + kBlock - 1) / kBlock;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    conv1d_kernel<TIO, VEC, K, kFast><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(p);
     return cudaGetLastError();
 }
-
 template <typename TIO, int VEC> cudaError_t launch_vec(const Conv1dParams &p, cudaStream_t st) {
     switch (p.width) {
         case 1: return launch_k<TIO, VEC, 1>(p, st);

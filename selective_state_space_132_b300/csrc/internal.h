@@ -84,6 +84,18 @@ struct SSDDecodeParams {
 };
 cudaError_t launch_ssd_decode(const SSDDecodeParams &p, cudaStream_t stream);
 
+struct ScanBwdParams {
+    int64_t batch, seqlen, dim, dstate;
+    int io_bf16, softplus, zoh;
+    const void *x, *delta, *B, *C, *z, *dy;
+    const float *A, *D, *bias, *h0, *dh_final;
+    void *dx, *ddelta, *dz;
+    float *dA, *dB, *dC, *dD, *ddelta_bias, *dh0;
+    float *ckpt;   // (B, ntiles, D, N) states at the tile starts
+};
+size_t scan_bwd_ckpt_floats(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate);
+cudaError_t launch_scan_bwd(const ScanBwdParams &p, cudaStream_t stream);
+
 struct Conv1dParams {
     int64_t batch, seqlen, dim, width;
     int io_bf16;

@@ -196,6 +196,57 @@ ssm_status check_ssd_decode(const ssm_ssd_decode_args *a) {
     return SSM_OK;
 }
 
+// ------------------------------------------------------------------ scan backward
+ssm_status check_scan_bwd(const ssm_scan_bwd_args *a, bool pointers = true) {
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->batch < 0 || a->seqlen < 0 || a->dim < 0 || a->dstate < 1) return SSM_ERR_INVALID_ARG;
+    if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+    if (a->delta_softplus != 0 && a->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (a->discretization != SSM_DISC_EULER && a->discretization != SSM_DISC_ZOH)
+        return SSM_ERR_INVALID_ARG;
+    if (a->dstate > 64) return SSM_ERR_UNSUPPORTED;
+    if (a->batch > 65535) return SSM_ERR_UNSUPPORTED;
+    if (a->seqlen > (int64_t)1 << 40 || a->dim > (int64_t)1 << 31) return SSM_ERR_UNSUPPORTED;
+    if (!pointers) return SSM_OK;
+    const bool tokens = a->batch * a->seqlen * a->dim > 0;
+    if (tokens && (!a->x || !a->delta || !a->B || !a->C || !a->dy || !a->dx || !a->ddelta ||
+                   !a->dB || !a->dC))
+        return SSM_ERR_INVALID_ARG;
+    if (tokens && (a->z != nullptr) != (a->dz != nullptr)) return SSM_ERR_INVALID_ARG;
+    if (a->dim > 0 && (!a->A || !a->dA)) return SSM_ERR_INVALID_ARG;
+    const size_t e = io_size(a->io_dtype);
+    const void *io_ptrs[] = {a->x, a->delta, a->B, a->C, a->z, a->dy, a->dx, a->ddelta, a->dz};
+    for (const void *p : io_ptrs)
+        if (!aligned(p, e)) return SSM_ERR_ALIGNMENT;
+    const void *f_ptrs[] = {a->A, a->D, a->delta_bias, a->h0, a->dh_final, a->dA, a->dB,
+                            a->dC, a->dD, a->ddelta_bias, a->dh0};
+    for (const void *p : f_ptrs)
+        if (!aligned(p, 4)) return SSM_ERR_ALIGNMENT;
+    const size_t tok = (size_t)(a->batch * a->seqlen * a->dim) * e;
+    const size_t bc_io = (size_t)(a->batch * a->seqlen * a->dstate) * e;
+    const size_t bc32 = (size_t)(a->batch * a->seqlen * a->dstate) * 4;
+    const size_t st = (size_t)(a->batch * a->dim * a->dstate) * 4;
+    const size_t dn = (size_t)(a->dim * a->dstate) * 4, d4 = (size_t)a->dim * 4;
+    struct Buf { const void *p; size_t n; };
+    const Buf ins[] = {{a->x, tok}, {a->delta, tok}, {a->B, bc_io}, {a->C, bc_io}, {a->z, tok},
+                       {a->A, dn}, {a->D, d4}, {a->delta_bias, d4}, {a->h0, st},
+                       {a->dy, tok}, {a->dh_final, st}};
+    const Buf outs[] = {{a->dx, tok}, {a->ddelta, tok}, {a->dz, tok}, {a->dA, dn}, {a->dB, bc32},
+                        {a->dC, bc32}, {a->dD, d4}, {a->ddelta_bias, d4}, {a->dh0, st}};
+    for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+        for (const Buf &in : ins)
+            if (overlaps(outs[i].p, outs[i].n, in.p, in.n)) return SSM_ERR_INVALID_ARG;
+        for (size_t j = 0; j < i; ++j)
+            if (overlaps(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return SSM_ERR_INVALID_ARG;
+    }
+    return SSM_OK;
+}
+
+size_t scan_bwd_ws(const ssm_scan_bwd_args *a) {
+    const size_t ck = ssm::scan_bwd_ckpt_floats(a->batch, a->seqlen, a->dim, a->dstate) * 4;
+    return ssm::kStatusBytes + (ck + 255) / 256 * 256;
+}
+
 // ------------------------------------------------------------------ conv1d
 ssm_status check_conv1d(const ssm_conv1d_args *a) {
     if (!a) return SSM_ERR_INVALID_ARG;
@@ -203,7 +254,6 @@ ssm_status check_conv1d(const ssm_conv1d_args *a) {
     if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
     if (a->silu != 0 && a->silu != 1) return SSM_ERR_INVALID_ARG;
     if (a->width > ssm::conv1d_max_width()) return SSM_ERR_UNSUPPORTED;
-    if (a->batch > 65535 || (a->seqlen + 63) / 64 > 65535) return SSM_ERR_UNSUPPORTED;
     const bool work = a->batch * a->seqlen * a->dim > 0;
     if (work && (!a->x || !a->out || !a->weight)) return SSM_ERR_INVALID_ARG;
     const size_t e = io_size(a->io_dtype);
@@ -382,6 +432,82 @@ ssm_status ssm_ssd_step_decode(const ssm_ssd_decode_args *a, ssm_stream_t stream
     p.bias = a->delta_bias;
     p.y = a->y;
     return from_cuda(ssm::launch_ssd_decode(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ssm_status ssm_scan_bwd_workspace_size(const ssm_scan_bwd_args *a, size_t *bytes) {
+    if (!bytes) return SSM_ERR_INVALID_ARG;
+    ssm_status s = check_scan_bwd(a, false);
+    if (s != SSM_OK) return s;
+    *bytes = scan_bwd_ws(a);
+    return SSM_OK;
+}
+
+ssm_status ssm_scan_bwd(const ssm_scan_bwd_args *a, ssm_stream_t stream) {
+    ssm_status s = check_scan_bwd(a);
+    if (s != SSM_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t rows = a->batch * a->seqlen;
+    // the sums start at zero; with no channels or no rows only they are written
+    if (a->dim > 0 && a->dA) {
+        if (cudaMemsetAsync(a->dA, 0, (size_t)(a->dim * a->dstate) * 4, st) != cudaSuccess)
+            return SSM_ERR_CUDA;
+    }
+    if (a->dD && cudaMemsetAsync(a->dD, 0, (size_t)a->dim * 4, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (a->ddelta_bias && cudaMemsetAsync(a->ddelta_bias, 0, (size_t)a->dim * 4, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (rows > 0) {
+        const size_t bc = (size_t)(rows * a->dstate) * 4;
+        if (cudaMemsetAsync(a->dB, 0, bc, st) != cudaSuccess ||
+            cudaMemsetAsync(a->dC, 0, bc, st) != cudaSuccess)
+            return SSM_ERR_CUDA;
+    }
+    if (a->batch * a->dim == 0) return SSM_OK;
+    if (a->seqlen == 0) {
+        // no steps: dh0 = dh_final
+        if (a->dh0) {
+            const size_t st_bytes = (size_t)(a->batch * a->dim * a->dstate) * 4;
+            cudaError_t e = a->dh_final
+                                ? cudaMemcpyAsync(a->dh0, a->dh_final, st_bytes,
+                                                  cudaMemcpyDeviceToDevice, st)
+                                : cudaMemsetAsync(a->dh0, 0, st_bytes, st);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    const size_t need = scan_bwd_ws(a);
+    if (!a->workspace || a->workspace_bytes < need) return SSM_ERR_WORKSPACE;
+    if (!aligned(a->workspace, 256)) return SSM_ERR_ALIGNMENT;
+    ssm::ScanBwdParams p{};
+    p.batch = a->batch;
+    p.seqlen = a->seqlen;
+    p.dim = a->dim;
+    p.dstate = a->dstate;
+    p.io_bf16 = a->io_dtype == SSM_BF16;
+    p.softplus = a->delta_softplus;
+    p.zoh = a->discretization == SSM_DISC_ZOH;
+    p.x = a->x;
+    p.delta = a->delta;
+    p.B = a->B;
+    p.C = a->C;
+    p.z = a->z;
+    p.dy = a->dy;
+    p.A = a->A;
+    p.D = a->D;
+    p.bias = a->delta_bias;
+    p.h0 = a->h0;
+    p.dh_final = a->dh_final;
+    p.dx = a->dx;
+    p.ddelta = a->ddelta;
+    p.dz = a->dz;
+    p.dA = a->dA;
+    p.dB = a->dB;
+    p.dC = a->dC;
+    p.dD = a->dD;
+    p.ddelta_bias = a->ddelta_bias;
+    p.dh0 = a->dh0;
+    p.ckpt = reinterpret_cast<float *>(static_cast<char *>(a->workspace) + ssm::kStatusBytes);
+    return from_cuda(ssm::launch_scan_bwd(p, st));
 }
 
 ssm_status ssm_conv1d(const ssm_conv1d_args *a, ssm_stream_t stream) {

@@ -35,7 +35,8 @@ def test_header_declares_expected_entry_points():
     fns = header_functions()
     for name in ("ssm_scan_fwd", "ssm_ssd_chunk_fwd", "ssm_step_decode", "ssm_ssd_plan",
                  "ssm_scan_workspace_size", "ssm_ssd_workspace_size", "ssm_status_string",
-                 "ssm_version", "ssm_read_device_status", "ssm_conv1d"):
+                 "ssm_version", "ssm_read_device_status", "ssm_conv1d", "ssm_scan_bwd",
+                 "ssm_scan_bwd_workspace_size"):
         assert name in fns
 
 
@@ -202,6 +203,41 @@ def test_ssd_decode_rejects_bad_arguments(lib):
     assert rc(x=0x200001) == ALIGN
     assert rc(y=0x200000) == INVALID                 # y aliases x
     assert rc(batch=0) == OK                         # nothing to do, nothing launched
+
+
+def test_scan_bwd_rejects_bad_arguments(lib):
+    def args(**kw):
+        base = dict(batch=2, seqlen=64, dim=32, dstate=16, io_dtype=1, delta_softplus=1,
+                    discretization=0, reserved=0, x=0x100000, delta=0x200000, B=0x300000,
+                    C=0x400000, z=None, A=0x500000, D=None, delta_bias=None, h0=None,
+                    dy=0x600000, dh_final=None, dx=0x700000, ddelta=0x800000, dz=None,
+                    dA=0x900000, dB=0xa00000, dC=0xb00000, dD=None, ddelta_bias=None,
+                    dh0=None, workspace=None, workspace_bytes=0)
+        base.update(kw)
+        return bd.ScanBwdArgs(**base)
+
+    def rc(**kw):
+        a = args(**kw)
+        return lib.ssm_scan_bwd(ctypes.byref(a), None)
+    assert lib.ssm_scan_bwd(None, None) == INVALID
+    assert rc(dstate=0) == INVALID
+    assert rc(dstate=65) == UNSUPPORTED
+    assert rc(discretization=3) == INVALID
+    assert rc(dy=None) == INVALID
+    assert rc(dB=None) == INVALID
+    assert rc(z=0xc00000) == INVALID                 # z without dz
+    assert rc(dz=0xc00000) == INVALID                # dz without z
+    assert rc(dx=0x100001) == ALIGN
+    assert rc(dA=0x900002) == ALIGN
+    assert rc(dx=0x100000) == INVALID                # dx aliases x
+    assert rc(ddelta=0x700010) == INVALID            # two outputs overlap
+    assert rc(dB=0x200000) == INVALID                # output over an input
+    need = ctypes.c_size_t(0)
+    a = args()
+    assert lib.ssm_scan_bwd_workspace_size(ctypes.byref(a), ctypes.byref(need)) == OK
+    # status word + one state per (b, 16-step tile, d): 2 * 4 * 32 * 16 floats
+    assert need.value == 256 + 2 * 4 * 32 * 16 * 4
+    assert ssm.scan_bwd_workspace_size(8, 2048, 1536, 16) == 256 + 8 * 128 * 1536 * 16 * 4
 
 
 def test_conv1d_rejects_bad_arguments(lib):

@@ -484,3 +484,125 @@ def test_conv1d_impulse_and_carried_window():
     first = oracle.conv1d(x[:, :11], w, silu=True)
     second = oracle.conv1d(x[:, 11:], w, x_prev=x[:, 11 - (K - 1):11], silu=True)
     np.testing.assert_allclose(np.concatenate([first, second], 1), full, rtol=1e-14, atol=1e-14)
+
+
+# ---------------------------------------------------------------- backward (adjoint) pins
+_GRAD_INPUTS = ("x", "delta", "A", "B", "C", "D", "z", "bias", "h0")
+
+
+def _bwd_problem(seed, zoh, nb=2, L=7, D=3, N=4):
+    rng = _rng(seed)
+    p = dict(x=rng.standard_normal((nb, L, D)), delta=0.5 * rng.standard_normal((nb, L, D)),
+             A=-rng.uniform(0.5, 4.0, (D, N)), B=rng.standard_normal((nb, L, N)),
+             C=rng.standard_normal((nb, L, N)), D=rng.standard_normal(D),
+             z=rng.standard_normal((nb, L, D)), bias=rng.uniform(-1.0, 0.5, D),
+             h0=rng.standard_normal((nb, D, N)))
+    if zoh:
+        p["A"][0, 1] = 0.0              # the A -> 0 limit of the zero-order hold
+        p["A"][1, 2] = -1e-4            # and its neighbourhood (series branch)
+    gy = rng.standard_normal((nb, L, D))
+    ghf = rng.standard_normal((nb, D, N))
+    return p, gy, ghf
+
+
+def _loss(p, gy, ghf, zoh):
+    y, hf = oracle.scan(p["x"], p["delta"], p["A"], p["B"], p["C"], Dv=p["D"], z=p["z"],
+                        bias=p["bias"], softplus=True, h0=p["h0"], zoh=zoh, threads=1)
+    return float(np.sum(gy * y) + np.sum(ghf * hf))
+
+
+def _bwd(p, gy, ghf, zoh):
+    g = oracle.scan_bwd(gy, p["x"], p["delta"], p["A"], p["B"], p["C"], Dv=p["D"], z=p["z"],
+                        bias=p["bias"], softplus=True, h0=p["h0"], gh_final=ghf, zoh=zoh)
+    return dict(x=g["gx"], delta=g["gdelta"], A=g["gA"], B=g["gB"], C=g["gC"], D=g["gD"],
+                z=g["gz"], bias=g["gbias"], h0=g["gh0"])
+
+
+@pytest.mark.parametrize("zoh", [False, True])
+def test_backward_equals_central_differences(zoh):
+    """Every gradient the adjoint returns equals the central difference of the forward
+    oracle's scalar loss <gy, y> + <gh_final, h_final>, element by element."""
+    p, gy, ghf = _bwd_problem(61 + zoh, zoh)
+    g = _bwd(p, gy, ghf, zoh)
+    eps = 1e-6
+    for name in _GRAD_INPUTS:
+        a = p[name]
+        fd = np.empty_like(a)
+        for i in np.ndindex(a.shape):
+            keep = a[i]
+            a[i] = keep + eps
+            up = _loss(p, gy, ghf, zoh)
+            a[i] = keep - eps
+            dn = _loss(p, gy, ghf, zoh)
+            a[i] = keep
+            fd[i] = (up - dn) / (2 * eps)
+        scale = max(1.0, float(np.max(np.abs(fd))))
+        assert np.max(np.abs(g[name] - fd)) < 2e-7 * scale, name
+
+
+def _torch_scan_loss(t, gy, ghf, zoh):
+    """A plain PyTorch fp64 restatement of the forward recurrence (own loop, no oracle
+    code), differentiated by autograd."""
+    import torch
+    x, dr, A, Bm, Cm, Dv, z, bias, h0 = (t[k] for k in _GRAD_INPUTS)
+    dl = torch.nn.functional.softplus(dr + bias)                       # (B,L,D)
+    h = h0
+    loss = 0.0
+    for s in range(x.shape[1]):
+        e = dl[:, s, :, None] * A[None]                                # (B,D,N)
+        if zoh:
+            # coef = dl * phi(e), phi(e) = (e^e - 1)/e, smooth through e = 0 (Taylor
+            # polynomial there) so that autograd sees the derivative at A = 0 too
+            small = e.abs() < 1e-3
+            e_safe = torch.where(small, torch.ones_like(e), e)
+            phi = torch.where(small, 1 + e / 2 + e * e / 6 + e * e * e / 24,
+                              torch.expm1(e_safe) / e_safe)
+            coef = dl[:, s, :, None] * phi
+        else:
+            coef = dl[:, s, :, None]
+        h = torch.exp(e) * h + coef * Bm[:, s, None, :] * x[:, s, :, None]
+        yr = (h * Cm[:, s, None, :]).sum(-1) + Dv * x[:, s]
+        y = yr * torch.nn.functional.silu(z[:, s])
+        loss = loss + (y * gy[:, s]).sum()
+    return loss + (h * ghf).sum()
+
+
+@pytest.mark.parametrize("zoh", [False, True])
+def test_backward_equals_autograd_of_an_independent_loop(zoh):
+    import torch
+    p, gy, ghf = _bwd_problem(71 + zoh, zoh, nb=3, L=40, D=6, N=8)
+    t = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True) for k, v in p.items()}
+    _torch_scan_loss(t, torch.tensor(gy), torch.tensor(ghf), zoh).backward()
+    g = _bwd(p, gy, ghf, zoh)
+    for name in _GRAD_INPUTS:
+        ref = t[name].grad.numpy()
+        assert oracle.rel_l2(g[name], ref) < 1e-12, name
+
+
+def test_backward_without_optional_inputs():
+    """No gate, no D, no bias, no h0, no softplus, no final-state gradient: gx then
+    equals the transposed semiseparable matrix applied to gy."""
+    rng = _rng(81)
+    nb, L, D, N = 1, 12, 2, 3
+    x = rng.standard_normal((nb, L, D))
+    dl = rng.uniform(0.05, 0.6, (nb, L, D))
+    A = -rng.uniform(0.5, 3.0, (D, N))
+    Bm, Cm = rng.standard_normal((nb, L, N)), rng.standard_normal((nb, L, N))
+    gy = rng.standard_normal((nb, L, D))
+    g = oracle.scan_bwd(gy, x, dl, A, Bm, Cm, softplus=False)
+    for d in range(D):
+        M = np.zeros((L, L))
+        for t_ in range(L):
+            for s in range(t_ + 1):
+                decay = np.exp(A[d] * dl[0, s + 1:t_ + 1, d].sum())
+                M[t_, s] = np.sum(Cm[0, t_] * decay * Bm[0, s]) * dl[0, s, d]
+        np.testing.assert_allclose(g["gx"][0, :, d], M.T @ gy[0, :, d], rtol=1e-12, atol=1e-12)
+    # gradients of the absent D and bias (taken at zero): sum gy x and sum gdelta
+    np.testing.assert_allclose(g["gD"], (gy * x).sum(axis=(0, 1)), rtol=1e-12)
+    np.testing.assert_allclose(g["gbias"], g["gdelta"].sum(axis=(0, 1)), rtol=1e-12)
+    # with no final-state gradient, gh0 = sum_t (prod_{r<=t} Abar_r) C_t gy_t
+    for d in range(D):
+        acc = np.zeros(N)
+        for t_ in range(L):
+            acc += np.exp(A[d] * dl[0, :t_ + 1, d].sum()) * Cm[0, t_] * gy[0, t_, d]
+        np.testing.assert_allclose(g["gh0"][0, d], acc, rtol=1e-12)
