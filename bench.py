@@ -390,6 +390,66 @@ def time_ssd_decode(nb, H, P, G, N, flush, device, iters=30):
     return float(np.median(times))
 
 
+def _median_event_time(step, flush, iters):
+    import torch
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e-3)
+    return float(np.median(times))
+
+
+def conv1d_bytes(nb, L, D, K, e):
+    return 2 * nb * L * D * e + D * K * 4 + D * 4
+
+
+def time_conv1d(nb, L, D, K, flush, device, iters=30):
+    """Median time of ssm_conv1d (causal depthwise Conv1D + SiLU), L2 flushed."""
+    import torch
+    import selective_state_space_132_b300 as ssm
+    rng = np.random.default_rng(1006)
+    t = _to_dev(device)
+    x = t(rng.standard_normal((nb, L, D), dtype=np.float32), torch.bfloat16)
+    w = t(rng.standard_normal((D, K), dtype=np.float32) / np.sqrt(K))
+    bias = t(rng.standard_normal(D, dtype=np.float32) * 0.1)
+    out = torch.empty_like(x)
+    return _median_event_time(lambda: ssm.conv1d(x, w, bias, out=out), flush, iters)
+
+
+def scan_bwd_bytes(nb, L, D, N, e, gate=True):
+    """Each input read once (x, delta, z, dy; B, C; A, D, bias), each gradient written
+    once (dx, ddelta, dz in the I/O type; dB, dC, dA, dD, dbias in fp32)."""
+    tok = nb * L * D * e
+    return (4 if gate else 3) * tok + 2 * nb * L * N * e + (3 if gate else 2) * tok \
+        + 2 * nb * L * N * 4 + 2 * D * N * 4 + 4 * D * 4
+
+
+def time_scan_bwd(p, flush, device, iters=10):
+    """Median time of one ssm_scan_bwd call (states recomputed) on the scan problem p,
+    including the zeroing of the summed gradients, L2 flushed before each call."""
+    import torch
+    import selective_state_space_132_b300 as ssm
+    t = _to_dev(device)
+    io = torch.bfloat16 if p.io == "bf16" else torch.float32
+    x, dl, z = t(p.x, io), t(p.delta, io), t(p.z, io)
+    Bm, Cm = t(p.B, io), t(p.C, io)
+    A, Dv, bias = t(p.A), t(p.D), t(p.bias)
+    dy = torch.randn_like(x)
+    ws = torch.empty(ssm.scan_bwd_workspace_size(p.batch, p.seqlen, p.dim, p.dstate, io),
+                     dtype=torch.uint8, device=device)
+    return _median_event_time(
+        lambda: ssm.scan_bwd(dy, x, dl, A, Bm, Cm, D=Dv, z=z, delta_bias=bias, workspace=ws),
+        flush, iters)
+
+
 def cpu_baseline_scan(p, target_s=10.0, max_s=30.0):
     """The fp64 oracle as it stands, all host cores, on a bounded channel sample of
     the workload; returns updates/s and what the sample was."""
@@ -477,45 +537,79 @@ def run_ours(args, world, rank, local):
     return out
 
 
-def extras(device, flush, hbm, tf_sus):
-    """The other workloads, one measurement each (parity cases, not the bench line)."""
+def extras(device, flush, hbm, tf_sus, only=None, iters=None):
+    """The other workloads, one measurement each (parity cases, not the bench line).
+    `only` runs one of them alone and `iters` sets its timed iterations (both used to
+    profile one kernel with ncu)."""
     import torch
+
+    def n(default):
+        return default if iters is None else iters
+
+    def scan_long():
+        p = W.config_problem(2)
+        per, launches, _, _ = time_scan(p, n(5), 3, flush, device)
+        s = float(np.median(per))
+        b = scan_bytes(p.batch, p.seqlen, p.dim, p.dstate, 2)
+        return {"ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
+                "hbm_frac": b / s / 1e9 / hbm, "launches": launches}
+
+    def ssd():
+        p = W.config_problem(3)
+        s = time_ssd(p, n(5), flush, device)
+        b = ssd_bytes(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, 2)
+        # the tensor-core kernel works in 128-step chunks whatever chunk_size asks for
+        fl = ssd_flops(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, 128)
+        return {"ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
+                "hbm_frac": b / s / 1e9 / hbm, "tensor_tflops": fl / s / 1e12,
+                "tensor_frac_sustained": fl / s / 1e12 / tf_sus, "kernel_chunk": 128}
+
+    def decode():
+        p = W.config_problem(4)
+        steps = p.steps if iters is None else iters
+        s_flush, s_hot = time_decode(p, steps, flush, device)
+        b = decode_bytes_per_step(p.batch, p.dim, p.dstate, 2)
+        return {"ms_per_step_l2_flushed": s_flush * 1e3, "ms_per_step_back_to_back": s_hot * 1e3,
+                "updates_per_s": p.updates_per_step / s_flush,
+                "gbs_l2_flushed": b / s_flush / 1e9, "hbm_frac_l2_flushed": b / s_flush / 1e9 / hbm,
+                "gbs_back_to_back": b / s_hot / 1e9,
+                "note": "back-to-back steps keep much of the 84 MB state in the 126 MB L2"}
+
+    def ssd_decode():
+        s = time_ssd_decode(64, 80, 64, 1, 128, flush, device, iters=n(30))
+        b = ssd_decode_bytes_per_step(64, 80, 64, 1, 128, 2)
+        return {"ms_per_step_l2_flushed": s * 1e3, "updates_per_s": 64 * 80 * 64 * 128 / s,
+                "gbs_l2_flushed": b / s / 1e9, "hbm_frac_l2_flushed": b / s / 1e9 / hbm}
+
+    def conv1d():
+        s = time_conv1d(8, 2048, 1536, 4, flush, device, iters=n(30))
+        b = conv1d_bytes(8, 2048, 1536, 4, 2)
+        return {"ms": s * 1e3, "gbs": b / s / 1e9, "hbm_frac": b / s / 1e9 / hbm}
+
+    def scan_bwd():
+        p = W.config_problem(1)
+        s = time_scan_bwd(p, flush, device, iters=n(10))
+        b = scan_bwd_bytes(p.batch, p.seqlen, p.dim, p.dstate, 2)
+        return {"ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
+                "hbm_frac": b / s / 1e9 / hbm,
+                "note": "states recomputed: a checkpoint pass and a reverse pass"}
+
+    runners = {
+        "scan_bf16_B1_D2048_L131072_N16": scan_long,
+        "ssd_bf16_B4_L8192_H80_P64_N128_G1_Q256": ssd,
+        "decode_bf16_B256_D5120_N16_x1000": decode,
+        "ssd_decode_bf16_B64_H80_P64_N128": ssd_decode,
+        "conv1d_silu_bf16_B8_L2048_D1536_K4": conv1d,
+        "scan_bwd_bf16_B8_D1536_L2048_N16": scan_bwd,
+    }
+    if only is not None and only not in runners:
+        raise SystemExit(f"unknown extra {only!r}; one of {sorted(runners)}")
     res = {}
-    p = W.config_problem(2)
-    per, launches, _, _ = time_scan(p, 5, 3, flush, device)
-    s = float(np.median(per))
-    b = scan_bytes(p.batch, p.seqlen, p.dim, p.dstate, 2)
-    res["scan_bf16_B1_D2048_L131072_N16"] = {
-        "ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
-        "hbm_frac": b / s / 1e9 / hbm, "launches": launches}
-    del p
-    p = W.config_problem(3)
-    s = time_ssd(p, 5, flush, device)
-    b = ssd_bytes(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, 2)
-    # the tensor-core kernel works in 128-step chunks whatever chunk_size asks for
-    fl = ssd_flops(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, 128)
-    res["ssd_bf16_B4_L8192_H80_P64_N128_G1_Q256"] = {
-        "ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
-        "hbm_frac": b / s / 1e9 / hbm, "tensor_tflops": fl / s / 1e12,
-        "tensor_frac_sustained": fl / s / 1e12 / tf_sus, "kernel_chunk": 128}
-    del p
-    torch.cuda.empty_cache()
-    p = W.config_problem(4)
-    s_flush, s_hot = time_decode(p, p.steps, flush, device)
-    b = decode_bytes_per_step(p.batch, p.dim, p.dstate, 2)
-    res["decode_bf16_B256_D5120_N16_x1000"] = {
-        "ms_per_step_l2_flushed": s_flush * 1e3, "ms_per_step_back_to_back": s_hot * 1e3,
-        "updates_per_s": p.updates_per_step / s_flush, "gbs_l2_flushed": b / s_flush / 1e9,
-        "hbm_frac_l2_flushed": b / s_flush / 1e9 / hbm,
-        "gbs_back_to_back": b / s_hot / 1e9,
-        "note": "back-to-back steps keep much of the 84 MB state in the 126 MB L2"}
-    del p
-    torch.cuda.empty_cache()
-    s = time_ssd_decode(64, 80, 64, 1, 128, flush, device)
-    b = ssd_decode_bytes_per_step(64, 80, 64, 1, 128, 2)
-    res["ssd_decode_bf16_B64_H80_P64_N128"] = {
-        "ms_per_step_l2_flushed": s * 1e3, "updates_per_s": 64 * 80 * 64 * 128 / s,
-        "gbs_l2_flushed": b / s / 1e9, "hbm_frac_l2_flushed": b / s / 1e9 / hbm}
+    for name, fn in runners.items():
+        if only is not None and name != only:
+            continue
+        res[name] = fn()
+        torch.cuda.empty_cache()
     return res
 
 
@@ -579,7 +673,19 @@ def main(argv=None):
                     default="scan_bf16_B8_D1536_L2048_N16")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--only-extra", default=None,
+                    help="run one of the other workloads alone and print its measurement")
+    ap.add_argument("--extra-iters", type=int, default=None,
+                    help="timed iterations of --only-extra (after 3 warm-up calls)")
     args = ap.parse_args(argv)
+    if args.only_extra is not None:
+        import torch
+        device = torch.device("cuda", 0)
+        hbm, _, tf_sus, _ = measured_peaks()
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        res = extras(device, flush, hbm, tf_sus, only=args.only_extra, iters=args.extra_iters)
+        print(json.dumps({"extra": args.only_extra, **res[args.only_extra]}))
+        return 0
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     if args.impl == "reference":

@@ -7,8 +7,9 @@
 //
 // B300 mapping: one read of x and one write of out, so HBM bound.  A thread owns a
 // 16-byte chunk of channels (8 bf16 or 4 fp32) of one batch row and walks a run of
-// kT time steps, keeping the last K - 1 inputs in registers and eight rows of loads in
-// flight; a warp reads and writes 512 contiguous bytes per row.  The K taps of its
+// 32 time steps in four batches of 8 rows, loading each batch while the previous one
+// is computed (two register buffers), and keeps the last K - 1 inputs in registers;
+// a warp reads and writes 512 contiguous bytes per row.  The K taps of its
 // channels stay in registers.
 // Shapes whose rows cannot be split into aligned 16-byte chunks run one channel per
 // thread.
@@ -19,14 +20,16 @@ namespace ssm {
 namespace {
 
 constexpr int kBlock = 128;
-constexpr int kT = 32;     // time steps per thread
-constexpr int kR = 8;      // rows loaded ahead (in flight per thread)
+constexpr int kR = 8;      // rows per batch: one batch is loaded while the previous computes
+constexpr int kNB = 4;     // batches per thread
+constexpr int kT = kR * kNB;   // time steps per thread
 constexpr int kMaxK = 8;
 
 // Raw 16-byte (or one-element) rows and their widening to fp32.
 template <typename TIO, int VEC> struct Vec;
 template <> struct Vec<__nv_bfloat16, 8> {
     using Raw = uint4;
+    static __device__ __forceinline__ Raw zero() { return make_uint4(0, 0, 0, 0); }
     static __device__ __forceinline__ Raw load(const __nv_bfloat16 *p) {
         return __ldg(reinterpret_cast<const uint4 *>(p));
     }
@@ -51,6 +54,7 @@ template <> struct Vec<__nv_bfloat16, 8> {
 };
 template <> struct Vec<float, 4> {
     using Raw = float4;
+    static __device__ __forceinline__ Raw zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
     static __device__ __forceinline__ Raw load(const float *p) {
         return __ldg(reinterpret_cast<const float4 *>(p));
     }
@@ -63,6 +67,7 @@ template <> struct Vec<float, 4> {
 };
 template <typename TIO> struct Vec<TIO, 1> {
     using Raw = TIO;
+    static __device__ __forceinline__ Raw zero() { return Io<TIO>::from_f(0.f); }
     static __device__ __forceinline__ Raw load(const TIO *p) { return *p; }
     static __device__ __forceinline__ void widen(const Raw &q, float (&v)[1]) {
         v[0] = Io<TIO>::to_f(q);
@@ -99,30 +104,38 @@ __global__ void __launch_bounds__(kBlock) conv1d_kernel(Conv1dParams p) {
         for (int k = 0; k < K; ++k) w[v][k] = in ? p.weight[(d0 + v) * K + k] : 0.f;
         bias[v] = (in && p.bias) ? p.bias[d0 + v] : 0.f;
     }
-    // win[k] holds x at t - (K - 1) + k for the step about to be computed
-    float win[K][VEC];
+    // the K - 1 inputs before t0 and the first batch of rows are loaded together; each
+    // later batch is loaded before the previous one is computed (two register buffers)
+    typename V::Raw halo[K > 1 ? K - 1 : 1], cur[kR], nxt[kR];
 #pragma unroll
     for (int k = 0; k < K - 1; ++k) {
         const int64_t s = t0 - (K - 1) + k;
-        if (s >= 0) {
-            V::widen(V::load(gx + (b * L + s) * D + d0), win[k]);
-        } else if (gprev) {
-            V::widen(V::load(gprev + (b * (K - 1) + (K - 1 + s)) * D + d0), win[k]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) win[k][e] = 0.f;
-        }
+        if (s >= 0) halo[k] = V::load(gx + (b * L + s) * D + d0);
+        else if (gprev) halo[k] = V::load(gprev + (b * (K - 1) + (K - 1 + s)) * D + d0);
+        else halo[k] = V::zero();
     }
-    const int64_t t1 = min(L, t0 + kT);
-    for (int64_t ta = t0; ta < t1; ta += kR) {
-        typename V::Raw raw[kR];
+    const int nrows = static_cast<int>(min(static_cast<int64_t>(kT), L - t0));
 #pragma unroll
-        for (int r = 0; r < kR; ++r)
-            if (ta + r < t1) raw[r] = V::load(gx + (b * L + ta + r) * D + d0);
+    for (int r = 0; r < kR; ++r)
+        if (r < nrows) cur[r] = V::load(gx + (b * L + t0 + r) * D + d0);
+    // win[k] holds x at t - (K - 1) + k for the step about to be computed
+    float win[K][VEC];
+#pragma unroll
+    for (int k = 0; k < K - 1; ++k) V::widen(halo[k], win[k]);
+#pragma unroll
+    for (int bi = 0; bi < kNB; ++bi) {
+        if (bi + 1 < kNB) {
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                const int rr = (bi + 1) * kR + r;
+                if (rr < nrows) nxt[r] = V::load(gx + (b * L + t0 + rr) * D + d0);
+            }
+        }
 #pragma unroll
         for (int r = 0; r < kR; ++r) {
-            if (ta + r < t1) {
-                V::widen(raw[r], win[K - 1]);
+            const int rr = bi * kR + r;
+            if (rr < nrows) {
+                V::widen(cur[r], win[K - 1]);
                 float out[VEC];
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
@@ -131,13 +144,15 @@ __global__ void __launch_bounds__(kBlock) conv1d_kernel(Conv1dParams p) {
                     for (int k = 0; k < K; ++k) acc = fmaf(w[e][k], win[k][e], acc);
                     out[e] = p.silu ? silu<kFast>(acc) : acc;
                 }
-                V::store(gout + (b * L + ta + r) * D + d0, out);
+                V::store(gout + (b * L + t0 + rr) * D + d0, out);
 #pragma unroll
                 for (int k = 0; k < K - 1; ++k)
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) win[k][e] = win[k + 1][e];
             }
         }
+#pragma unroll
+        for (int r = 0; r < kR; ++r) cur[r] = nxt[r];
     }
 }
 

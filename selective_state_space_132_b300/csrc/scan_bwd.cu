@@ -30,6 +30,7 @@
 //   the sequence and added atomically at the end.
 #include "../../include/ssm.h"
 #include "common.cuh"
+#include "ptx.cuh"
 #include "internal.h"
 
 namespace ssm {
@@ -41,6 +42,7 @@ constexpr int kThreads = 128;
 template <int NS> struct BwdShape {
     static constexpr int NP = 4 * NS;                            // padded state count
     static constexpr int T = NS <= 2 ? 32 : 64 / NS;             // steps per tile
+    static_assert(NS % 2 == 0, "states are processed in packed pairs");
     static constexpr int kRows = 9;                              // per-(t, channel) arrays
     static constexpr size_t floats = static_cast<size_t>(T) * kCB * NP   // states
                                      + 2 * T * NP                        // B, C
@@ -83,6 +85,41 @@ __device__ __forceinline__ void halve(const float *v, float *o, int mask, bool u
     }
 }
 
+using ptx::f2;
+using ptx::fma2;
+using ptx::mul2;
+
+template <bool kFast> __device__ __forceinline__ f2 decay2(f2 dl2, f2 a2) {
+    const f2 e = mul2(dl2, a2);
+    if (kFast) return f2{ex2_approx(e.x), ex2_approx(e.y)};
+    return f2{expf(e.x), expf(e.y)};
+}
+
+// NH pairs of consecutive floats from shared memory (8- or 16-byte aligned).
+template <int NH> __device__ __forceinline__ void ld_pairs(const float *p, f2 (&o)[NH]) {
+    if constexpr (NH == 1) {
+        const float2 v = *reinterpret_cast<const float2 *>(p);
+        o[0] = f2{v.x, v.y};
+    } else {
+#pragma unroll
+        for (int i = 0; i < NH / 2; ++i) {
+            const float4 v = reinterpret_cast<const float4 *>(p)[i];
+            o[2 * i] = f2{v.x, v.y};
+            o[2 * i + 1] = f2{v.z, v.w};
+        }
+    }
+}
+template <int NH> __device__ __forceinline__ void st_pairs(float *p, const f2 (&o)[NH]) {
+    if constexpr (NH == 1) {
+        *reinterpret_cast<float2 *>(p) = make_float2(o[0].x, o[0].y);
+    } else {
+#pragma unroll
+        for (int i = 0; i < NH / 2; ++i)
+            reinterpret_cast<float4 *>(p)[i] = make_float4(o[2 * i].x, o[2 * i].y,
+                                                           o[2 * i + 1].x, o[2 * i + 1].y);
+    }
+}
+
 template <typename TIO> __device__ __forceinline__ float ld_io(const void *p, int64_t i) {
     return Io<TIO>::load(static_cast<const TIO *>(p) + i);
 }
@@ -117,155 +154,246 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
     const bool dvalid = d < Dm;
     const int64_t nt = (L + T - 1) / T;
 
-    float A2[NS], An[NS], ia[NS];
+    constexpr int NH = NS / 2;           // state pairs of a lane
+    f2 A2[NH], An[NH], ia[NH];
     bool nval[NS];
 #pragma unroll
-    for (int j = 0; j < NS; ++j) {
-        const int64_t n = k * NS + j;
-        nval[j] = dvalid && n < N;
-        An[j] = nval[j] ? p.A[d * N + n] : 0.f;
-        A2[j] = scale_A<kFast>(An[j]);
-        ia[j] = An[j] != 0.f ? 1.f / An[j] : 0.f;
+    for (int q = 0; q < NH; ++q) {
+        float av[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int j = 2 * q + e;
+            const int64_t n = k * NS + j;
+            nval[j] = dvalid && n < N;
+            av[e] = nval[j] ? p.A[d * N + n] : 0.f;
+        }
+        An[q] = f2{av[0], av[1]};
+        A2[q] = f2{scale_A<kFast>(av[0]), scale_A<kFast>(av[1])};
+        ia[q] = f2{av[0] != 0.f ? 1.f / av[0] : 0.f, av[1] != 0.f ? 1.f / av[1] : 0.f};
     }
     const float Dd = (dvalid && p.D) ? p.D[d] : 0.f;
 
-    // ---- cooperative staging of a tile's rows and of B, C
+    // ---- staging of a tile's rows and of B, C, software-pipelined: the raw values of
+    // the next tile are loaded into registers before the current tile is computed and
+    // written to shared memory after it.
     // row element e = tid + 128 r: t = e / 32, channel cc = e % 32 = tid % 32
     const int cc = tid & 31;
     const int64_t dcc = dbase + cc;
     const bool ccvalid = dcc < Dm;
     const float bias_cc = (ccvalid && p.bias) ? p.bias[dcc] : 0.f;
-    auto stage = [&](int64_t t0, int Ts, bool full) {
-        for (int t = tid >> 5; t < T; t += kThreads / kCB) {
+    constexpr int kRowsPer = T / (kThreads / kCB);                 // rows per thread
+    constexpr int kBCPer = (T * NP + kThreads - 1) / kThreads;     // B/C elements per thread
+    const TIO zero_io = Io<TIO>::from_f(0.f);
+    struct Pre {
+        TIO x[kRowsPer], dt[kRowsPer], z[kRowsPer], gy[kRowsPer], B[kBCPer], C[kBCPer];
+    } pre;
+    auto prefetch = [&](int64_t t0, int Ts, bool full) {
+        const TIO *gx = static_cast<const TIO *>(p.x), *gd = static_cast<const TIO *>(p.delta);
+        const TIO *gz = static_cast<const TIO *>(p.z), *ggy = static_cast<const TIO *>(p.dy);
+        const TIO *gB = static_cast<const TIO *>(p.B), *gC = static_cast<const TIO *>(p.C);
+#pragma unroll
+        for (int r = 0; r < kRowsPer; ++r) {
+            const int t = (tid >> 5) + r * (kThreads / kCB);
             const bool in = t < Ts && ccvalid;
             const int64_t i = (b * L + t0 + t) * Dm + dcc;
-            const float xv = in ? ld_io<TIO>(p.x, i) : 0.f;
-            const float v = in ? ld_io<TIO>(p.delta, i) + bias_cc : 0.f;
-            sx[t * kCB + cc] = xv;
-            sdl[t * kCB + cc] = in ? (p.softplus ? softplus<kFast>(v) : v) : 0.f;
+            pre.x[r] = in ? __ldg(gx + i) : zero_io;
+            pre.dt[r] = in ? __ldg(gd + i) : zero_io;
             if (full) {
-                const float zv = (in && p.z) ? ld_io<TIO>(p.z, i) : 0.f;
-                const float gy = in ? ld_io<TIO>(p.dy, i) : 0.f;
+                pre.z[r] = (in && gz) ? __ldg(gz + i) : zero_io;
+                pre.gy[r] = in ? __ldg(ggy + i) : zero_io;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kBCPer; ++q) {
+            const int e = tid + q * kThreads;
+            const int t = e / NP, n = e % NP;
+            const bool in = e < T * NP && t < Ts && n < N;
+            const int64_t i = (b * L + t0 + t) * N + n;
+            pre.B[q] = in ? __ldg(gB + i) : zero_io;
+            if (full) pre.C[q] = in ? __ldg(gC + i) : zero_io;
+        }
+    };
+    auto commit = [&](bool full) {
+#pragma unroll
+        for (int r = 0; r < kRowsPer; ++r) {
+            const int t = (tid >> 5) + r * (kThreads / kCB);
+            const float xv = Io<TIO>::to_f(pre.x[r]);
+            const float v = Io<TIO>::to_f(pre.dt[r]) + bias_cc;
+            sx[t * kCB + cc] = xv;
+            sdl[t * kCB + cc] = ccvalid ? (p.softplus ? softplus<kFast>(v) : v) : 0.f;
+            if (full) {
+                const float zv = Io<TIO>::to_f(pre.z[r]);
+                const float gy = Io<TIO>::to_f(pre.gy[r]);
                 sv[t * kCB + cc] = v;
                 sz[t * kCB + cc] = zv;
                 sgy[t * kCB + cc] = gy;
                 sg[t * kCB + cc] = p.z ? gy * silu<kFast>(zv) : gy;
             }
         }
-        for (int e = tid; e < T * NP; e += kThreads) {
-            const int t = e / NP, n = e % NP;
-            const bool in = t < Ts && n < N;
-            const int64_t i = (b * L + t0 + t) * N + n;
-            sB[e] = in ? ld_io<TIO>(p.B, i) : 0.f;
-            if (full) sC[e] = in ? ld_io<TIO>(p.C, i) : 0.f;
+#pragma unroll
+        for (int q = 0; q < kBCPer; ++q) {
+            const int e = tid + q * kThreads;
+            if (e < T * NP) {
+                sB[e] = Io<TIO>::to_f(pre.B[q]);
+                if (full) sC[e] = Io<TIO>::to_f(pre.C[q]);
+            }
         }
     };
 
     // ---- 1. checkpoint pass
-    float h[NS];
+    // input term of the update for a pair: coefficient (dl or the ZOH one) x B x
+    auto input2 = [&](int q, f2 a, f2 Bp, float dl, float xv) -> f2 {
+        if (kZoh) {
+            const f2 cf{zoh_coef<kFast>(dl, dl * An[q].x, a.x, ia[q].x),
+                        zoh_coef<kFast>(dl, dl * An[q].y, a.y, ia[q].y)};
+            return mul2(mul2(cf, Bp), f2{xv, xv});
+        }
+        const float u = dl * xv;
+        return mul2(Bp, f2{u, u});
+    };
+    f2 h[NH];
 #pragma unroll
-    for (int j = 0; j < NS; ++j)
-        h[j] = (nval[j] && p.h0) ? p.h0[(b * Dm + d) * N + k * NS + j] : 0.f;
+    for (int q = 0; q < NH; ++q) {
+        const float *h0 = p.h0 + (b * Dm + d) * N + k * NS + 2 * q;
+        h[q] = f2{(nval[2 * q] && p.h0) ? h0[0] : 0.f, (nval[2 * q + 1] && p.h0) ? h0[1] : 0.f};
+    }
+    if (nt > 1) prefetch(0, T, false);
     for (int64_t s = 0; s < nt; ++s) {
         float *ck = p.ckpt + ((b * nt + s) * Dm + d) * N + k * NS;
 #pragma unroll
-        for (int j = 0; j < NS; ++j)
-            if (nval[j]) ck[j] = h[j];
+        for (int q = 0; q < NH; ++q) {
+            if (nval[2 * q]) ck[2 * q] = h[q].x;
+            if (nval[2 * q + 1]) ck[2 * q + 1] = h[q].y;
+        }
         if (s == nt - 1) break;                 // the last tile starts from this state
         __syncthreads();
-        stage(s * T, T, false);
+        commit(false);
+        if (s + 2 < nt) prefetch((s + 1) * T, T, false);
         __syncthreads();
+#pragma unroll 2
         for (int t = 0; t < T; ++t) {
             const float dl = sdl[t * kCB + c], xv = sx[t * kCB + c];
+            f2 Bp[NH];
+            ld_pairs<NH>(sB + t * NP + k * NS, Bp);
 #pragma unroll
-            for (int j = 0; j < NS; ++j) {
-                const float a = decay<kFast>(dl, A2[j]);
-                const float cf = kZoh ? zoh_coef<kFast>(dl, dl * An[j], a, ia[j]) : dl;
-                h[j] = fmaf(a, h[j], cf * xv * sB[t * NP + k * NS + j]);
+            for (int q = 0; q < NH; ++q) {
+                const f2 a = decay2<kFast>(f2{dl, dl}, A2[q]);
+                h[q] = fma2(a, h[q], input2(q, a, Bp[q], dl, xv));
             }
         }
     }
     // the checkpoint stores of this block are read back by the same threads below
 
     // ---- 2. reverse pass
-    float lam[NS], gA[NS];
+    f2 lam[NH], gA[NH];
 #pragma unroll
-    for (int j = 0; j < NS; ++j) {
-        lam[j] = (nval[j] && p.dh_final) ? p.dh_final[(b * Dm + d) * N + k * NS + j] : 0.f;
-        gA[j] = 0.f;
+    for (int q = 0; q < NH; ++q) {
+        const float *hf = p.dh_final + (b * Dm + d) * N + k * NS + 2 * q;
+        lam[q] = f2{(nval[2 * q] && p.dh_final) ? hf[0] : 0.f,
+                    (nval[2 * q + 1] && p.dh_final) ? hf[1] : 0.f};
+        gA[q] = f2{0.f, 0.f};
     }
     float gD_acc = 0.f, gbias_acc = 0.f;     // channel cc, rows of this thread
+    auto tile_len = [&](int64_t s) { return static_cast<int>(L - s * T < T ? L - s * T : T); };
+    f2 hst[NH], hst_next[NH];
+    auto load_ckpt = [&](int64_t s) {
+        const float *ck = p.ckpt + ((b * nt + s) * Dm + d) * N + k * NS;
+#pragma unroll
+        for (int q = 0; q < NH; ++q)
+            hst_next[q] = f2{nval[2 * q] ? __ldcg(ck + 2 * q) : 0.f,
+                             nval[2 * q + 1] ? __ldcg(ck + 2 * q + 1) : 0.f};
+    };
+    prefetch((nt - 1) * T, tile_len(nt - 1), true);
+    load_ckpt(nt - 1);
     for (int64_t s = nt - 1; s >= 0; --s) {
         const int64_t t0 = s * T;
-        const int Ts = static_cast<int>(L - t0 < T ? L - t0 : T);
+        const int Ts = tile_len(s);
         __syncthreads();
-        stage(t0, Ts, true);
-        float hst[NS];
-        {
-            const float *ck = p.ckpt + ((b * nt + s) * Dm + d) * N + k * NS;
+        commit(true);
 #pragma unroll
-            for (int j = 0; j < NS; ++j) hst[j] = nval[j] ? ck[j] : 0.f;
+        for (int q = 0; q < NH; ++q) hst[q] = hst_next[q];
+        if (s > 0) {
+            prefetch((s - 1) * T, T, true);
+            load_ckpt(s - 1);
         }
         __syncthreads();
         // recompute h_t of the tile (and C.h + D x for the gate's gradient)
 #pragma unroll
-        for (int j = 0; j < NS; ++j) h[j] = hst[j];
+        for (int q = 0; q < NH; ++q) h[q] = hst[q];
+#pragma unroll 2
         for (int t = 0; t < Ts; ++t) {
             const float dl = sdl[t * kCB + c], xv = sx[t * kCB + c];
-            float part = 0.f;
-            float *hrow = hs + (t * kCB + c) * NP + k * NS;
+            f2 Bp[NH], Cp[NH];
+            ld_pairs<NH>(sB + t * NP + k * NS, Bp);
+            ld_pairs<NH>(sC + t * NP + k * NS, Cp);
+            f2 part2{0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < NS; ++j) {
-                const float a = decay<kFast>(dl, A2[j]);
-                const float cf = kZoh ? zoh_coef<kFast>(dl, dl * An[j], a, ia[j]) : dl;
-                h[j] = fmaf(a, h[j], cf * xv * sB[t * NP + k * NS + j]);
-                part = fmaf(sC[t * NP + k * NS + j], h[j], part);
-                hrow[j] = h[j];
+            for (int q = 0; q < NH; ++q) {
+                const f2 a = decay2<kFast>(f2{dl, dl}, A2[q]);
+                h[q] = fma2(a, h[q], input2(q, a, Bp[q], dl, xv));
+                part2 = fma2(Cp[q], h[q], part2);
             }
+            st_pairs<NH>(hs + (t * kCB + c) * NP + k * NS, h);
+            float part = part2.x + part2.y;
             part += __shfl_xor_sync(0xffffffffu, part, 1);
             part += __shfl_xor_sync(0xffffffffu, part, 2);
             if (k == 0) syr[t * kCB + c] = fmaf(Dd, xv, part);
         }
         // walk the tile backwards; h holds h_t, hp is h_{t-1}
+#pragma unroll 2
         for (int t = Ts - 1; t >= 0; --t) {
-            float hp[NS];
+            f2 hp[NH];
             if (t > 0) {
-                const float *hrow = hs + ((t - 1) * kCB + c) * NP + k * NS;
-#pragma unroll
-                for (int j = 0; j < NS; ++j) hp[j] = hrow[j];
+                ld_pairs<NH>(hs + ((t - 1) * kCB + c) * NP + k * NS, hp);
             } else {
 #pragma unroll
-                for (int j = 0; j < NS; ++j) hp[j] = hst[j];
+                for (int q = 0; q < NH; ++q) hp[q] = hst[q];
             }
             const float g = sg[t * kCB + c], xv = sx[t * kCB + c], dl = sdl[t * kCB + c];
+            const f2 g2{g, g}, dl2{dl, dl};
+            f2 Bp[NH], Cp[NH];
+            ld_pairs<NH>(sB + t * NP + k * NS, Bp);
+            ld_pairs<NH>(sC + t * NP + k * NS, Cp);
             float pv[2 * NS];          // [0, NS): dB parts, [NS, 2NS): dC parts
-            float sLB = 0.f, gxp = 0.f, gdlp = 0.f;
+            f2 sLB2{0.f, 0.f}, gx2{0.f, 0.f}, gdl2{0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < NS; ++j) {
-                const float Bv = sB[t * NP + k * NS + j], Cv = sC[t * NP + k * NS + j];
-                pv[NS + j] = g * h[j];
-                lam[j] = fmaf(g, Cv, lam[j]);
-                const float a = decay<kFast>(dl, A2[j]);
-                const float q = lam[j] * hp[j] * a;
-                gdlp = fmaf(q, An[j], gdlp);
+            for (int q = 0; q < NH; ++q) {
+                const f2 pc = mul2(g2, h[q]);
+                pv[NS + 2 * q] = pc.x;
+                pv[NS + 2 * q + 1] = pc.y;
+                lam[q] = fma2(g2, Cp[q], lam[q]);
+                const f2 a = decay2<kFast>(dl2, A2[q]);
+                const f2 qq = mul2(mul2(lam[q], hp[q]), a);
+                gdl2 = fma2(qq, An[q], gdl2);
+                f2 pb;
                 if (kZoh) {
-                    const float v = dl * An[j];
-                    const float cf = zoh_coef<kFast>(dl, v, a, ia[j]);
-                    const float lc = lam[j] * cf;
-                    pv[j] = lc * xv;
-                    gxp = fmaf(lc, Bv, gxp);
-                    const float lbx = lam[j] * Bv * xv;
-                    gdlp = fmaf(lbx, a, gdlp);
-                    gA[j] = fmaf(q, dl, fmaf(lbx, zoh_dc_dA<kFast>(dl, v, a, ia[j]), gA[j]));
+                    const f2 v{dl * An[q].x, dl * An[q].y};
+                    const f2 cf{zoh_coef<kFast>(dl, v.x, a.x, ia[q].x),
+                                zoh_coef<kFast>(dl, v.y, a.y, ia[q].y)};
+                    const f2 lc = mul2(lam[q], cf);
+                    pb = mul2(lc, f2{xv, xv});
+                    gx2 = fma2(lc, Bp[q], gx2);
+                    const f2 lbx = mul2(mul2(lam[q], Bp[q]), f2{xv, xv});
+                    gdl2 = fma2(lbx, a, gdl2);
+                    const f2 dcda{zoh_dc_dA<kFast>(dl, v.x, a.x, ia[q].x),
+                                  zoh_dc_dA<kFast>(dl, v.y, a.y, ia[q].y)};
+                    gA[q] = fma2(qq, dl2, fma2(lbx, dcda, gA[q]));
                 } else {
-                    pv[j] = lam[j] * (dl * xv);
-                    sLB = fmaf(lam[j], Bv, sLB);
-                    gA[j] = fmaf(q, dl, gA[j]);
+                    const float u = dl * xv;
+                    pb = mul2(lam[q], f2{u, u});
+                    sLB2 = fma2(lam[q], Bp[q], sLB2);
+                    gA[q] = fma2(qq, dl2, gA[q]);
                 }
-                lam[j] *= a;
-                h[j] = hp[j];
+                pv[2 * q] = pb.x;
+                pv[2 * q + 1] = pb.y;
+                lam[q] = mul2(lam[q], a);
+                h[q] = hp[q];
             }
-            if (!kZoh) {
+            float gxp, gdlp = gdl2.x + gdl2.y;
+            if (kZoh) {
+                gxp = gx2.x + gx2.y;
+            } else {
+                const float sLB = sLB2.x + sLB2.y;
                 gxp = dl * sLB;
                 gdlp = fmaf(xv, sLB, gdlp);
             }
@@ -299,15 +427,6 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
                     const int m = (c8 >> 1);             // 2 b4 + b3
                     red[(m / NS) * NP + k * NS + m % NS] = r2[0];
                 }
-            } else {
-                float r1[1];
-                halve<1>(pv, r1, 16, lane & 16);
-                r1[0] += __shfl_xor_sync(0xffffffffu, r1[0], 8);
-                r1[0] += __shfl_xor_sync(0xffffffffu, r1[0], 4);
-                if (!(lane & 12)) {
-                    const int m = c8 >> 2;               // b4
-                    red[m * NP + k * NS] = r1[0];
-                }
             }
         }
         __syncthreads();
@@ -340,10 +459,14 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
     }
     // ---- per-channel and per-state sums
 #pragma unroll
-    for (int j = 0; j < NS; ++j) {
-        if (!nval[j]) continue;
-        atomicAdd(p.dA + d * N + k * NS + j, gA[j]);
-        if (p.dh0) p.dh0[(b * Dm + d) * N + k * NS + j] = lam[j];
+    for (int q = 0; q < NH; ++q) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int j = 2 * q + e;
+            if (!nval[j]) continue;
+            atomicAdd(p.dA + d * N + k * NS + j, e ? gA[q].y : gA[q].x);
+            if (p.dh0) p.dh0[(b * Dm + d) * N + k * NS + j] = e ? lam[q].y : lam[q].x;
+        }
     }
     __syncthreads();
     float *sacc = sm;                  // [4][kCB][2]
@@ -375,7 +498,6 @@ cudaError_t launch_ns(const ScanBwdParams &p, cudaStream_t stream) {
 
 template <typename TIO, bool kZoh>
 cudaError_t launch_typed(const ScanBwdParams &p, cudaStream_t stream) {
-    if (p.dstate <= 4) return launch_ns<TIO, 1, kZoh>(p, stream);
     if (p.dstate <= 8) return launch_ns<TIO, 2, kZoh>(p, stream);
     if (p.dstate <= 16) return launch_ns<TIO, 4, kZoh>(p, stream);
     if (p.dstate <= 32) return launch_ns<TIO, 8, kZoh>(p, stream);
@@ -383,7 +505,6 @@ cudaError_t launch_typed(const ScanBwdParams &p, cudaStream_t stream) {
 }
 
 int tile_steps(int64_t dstate) {
-    if (dstate <= 4) return BwdShape<1>::T;
     if (dstate <= 8) return BwdShape<2>::T;
     if (dstate <= 16) return BwdShape<4>::T;
     if (dstate <= 32) return BwdShape<8>::T;

@@ -11,24 +11,26 @@
 // our own for B300).
 //
 // B300 mapping
-//   * One warp per thread block.  The warp owns CPW = 32 / LPC channels of one
-//     batch row; each channel's N states are split over LPC adjacent lanes, NS
-//     states per lane.  The recurrence runs in time order inside each lane (one
-//     exp, two packed fp32x2 products and two packed FMAs per pair of states).
-//     Small single-warp blocks keep the 148 SMs evenly loaded (about ten blocks
-//     per SM at the 130M-layer shape) and need no block-wide barrier.
+//   * A block owns the 32 channels of one token-tile row (64 bytes of bf16, 128 of
+//     fp32) of one batch row: WPC warps of CPW = 32 / LPC channels each.  Each
+//     channel's N states are split over LPC adjacent lanes, NS states per lane.  The
+//     recurrence runs in time order inside each lane (one exp, one packed fp32x2
+//     product and one packed FMA per pair of states).  At the 130M-layer shape (N 16,
+//     LPC 4) that is 384 blocks of 4 warps, 3 blocks per SM.
 //   * Inputs arrive through a two-stage TMA pipeline: 3-D tensor maps over
-//     (channel, time, batch) give boxes of CPW channels x 32 steps for x, delta
-//     and z and N states x 32 steps for B and C; boxes past the end of a sequence
-//     are zero-filled by the TMA unit.  One lane issues the copies, every lane
-//     waits on the stage's mbarrier (bounded by a clock budget).
-//   * Per 32-step tile: (1) a prologue in which lane t turns row t of the tile
-//     into fp32 (dl, dl*x) pairs (softplus computed once per (t, d)) and converts
-//     B and C to fp32; (2) the scan, reading (dl, dl*x) with 16-byte loads and B,
-//     C as broadcast 16-byte loads; per-lane partial readouts go to shared
-//     memory; (3) an epilogue in which lane t sums the partials of row t, adds
-//     D x, applies the gate, rounds to the I/O type and writes a y tile that one
-//     TMA store sends to HBM.
+//     (channel, time, batch) give boxes of 32 channels x 32 steps for x, delta and z
+//     (64/128-byte swizzle) and N states x 32 steps for B and C; boxes past the end
+//     of a sequence are zero-filled by the TMA unit.  One thread issues the copies,
+//     every thread waits on the stage's mbarrier (bounded by a clock budget).
+//   * Per 32-step tile: (1) a prologue in which lane t turns row t of its warp's
+//     channels into fp32 (dl, dl*x) pairs (softplus computed once per (t, d));
+//     (2) the scan, reading (dl, dl*x) with 16-byte loads and B, C straight from the
+//     TMA tile (bf16 pairs widened in registers, or fp32) as broadcast loads;
+//     per-lane partial readouts go to shared memory; (3) an epilogue in which lane t
+//     sums the partials of row t, adds D x, applies the gate, rounds to the I/O type
+//     and writes a y tile that one TMA store sends to HBM.
+//   * The bound on B300 is the shared-memory to register traffic (B, C and the
+//     (dl, dl*x) pairs delivered to every lane), not HBM.
 //   * Long sequences are cut into K time chunks (blockIdx.z).  A summary pass
 //     (kSummary) scans chunks 0..K-2 from a zero state and keeps each chunk's end
 //     state and step sum; the output pass folds the summaries of earlier chunks
@@ -71,7 +73,9 @@ template <typename TIO, int NS, int LPC, int WPC, bool kSummary> struct Layout {
     static constexpr int ROWB = CPB * E;       // 32, 64 or 128 bytes (swizzle span)
     static constexpr int kTok = kT * ROWB;     // bytes of one x / delta / z tile
     static constexpr int kBC = kT * N * E;     // bytes of one B or C tile
-    static constexpr bool kConvBC = E != 4;    // bf16 B/C are widened to fp32 once
+    // bf16 B/C are read as bf16 pairs straight from the TMA tile and widened in
+    // registers (half the shared-memory bytes of fp32 copies); fp32 B/C as they are
+    static constexpr bool kRawBC = E == 2;
     // one pipeline stage: x, delta, z, B, C (no z, C in the summary pass)
     static constexpr int s_x = 0;
     static constexpr int s_dl = s_x + align1k(kTok);
@@ -86,13 +90,11 @@ template <typename TIO, int NS, int LPC, int WPC, bool kSummary> struct Layout {
     // fp32 (dl, dl x) pairs, one row of 2 kT floats per channel (16-byte aligned rows)
     static constexpr int kDlxRow = 2 * kT + 4;
     static constexpr int o_dlx = kStages * stage;
-    static constexpr int o_Bf = o_dlx + align1k(CPB * kDlxRow * 4);
-    static constexpr int o_Cf = o_Bf + (kConvBC ? align1k(kT * N * 4) : 0);
     // per warp: LPC slots of partial readouts [slot][t][channel], t-stride CPW + 4
     // (conflict-free row reads) and slot stride = 8 mod 32 (conflict-free writes)
     static constexpr int kPartT = CPW + 4;
     static constexpr int kPart = (kT * kPartT + 31) / 32 * 32 + 8;
-    static constexpr int o_part = o_Cf + ((kConvBC && !kSummary) ? align1k(kT * N * 4) : 0);
+    static constexpr int o_part = o_dlx + align1k(CPB * kDlxRow * 4);
     static constexpr int o_y = o_part + (kSummary ? 0 : align1k(WPC * LPC * kPart * 4));
     static constexpr int o_bar = o_y + (kSummary ? 0 : 2 * align1k(kTok));
     static constexpr int bytes = o_bar + kStages * 8 + 1024;  // + slack to align the base
@@ -266,10 +268,8 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
         const bool got = ptx::mbar_wait(&bars[s], (tile / kStages) & 1);
 
         // ---------------- prologue (only after this thread's own wait succeeded)
-        const float *Bf = reinterpret_cast<const float *>(LY::kConvBC ? smem + LY::o_Bf
-                                                                     : st + LY::s_B);
-        const float *Cf = reinterpret_cast<const float *>(LY::kConvBC ? smem + LY::o_Cf
-                                                                     : st + LY::s_C);
+        const float *Bf = reinterpret_cast<const float *>(st + LY::s_B);   // fp32 I/O
+        const float *Cf = reinterpret_cast<const float *>(st + LY::s_C);
         if (got) {
             const bool tval = t0 + lane < t_end;
 #pragma unroll
@@ -284,21 +284,6 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
                     const float dl = tval ? step_size<kFast>(vd[e], pbias[cc], p.softplus) : 0.f;
                     *reinterpret_cast<float2 *>(dlx + (warp * CPW + cc) * LY::kDlxRow + 2 * lane) =
                         make_float2(dl, kZoh ? vx[e] : dl * vx[e]);
-                }
-            }
-            if constexpr (LY::kConvBC) {
-                // B (and C) tiles to fp32, shared by the block: 16-byte chunks
-                constexpr int kChunksBC = LY::kBC / 16;
-                constexpr int kTot = (kSummary ? 1 : 2) * kChunksBC;
-                for (int q = tid; q < kTot; q += NT) {
-                    const bool isC = q >= kChunksBC;
-                    const int qq = isC ? q - kChunksBC : q;
-                    float v[EC];
-                    CK::load(st + (isC ? LY::s_C : LY::s_B) + qq * 16, v);
-                    float *dst = reinterpret_cast<float *>(smem + (isC ? LY::o_Cf : LY::o_Bf)) +
-                                 qq * EC;
-                    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-                    *reinterpret_cast<float4 *>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
                 }
             }
         }
@@ -321,6 +306,39 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
                 f2 bp[kU][NS / 2], cp[kU][NS / 2];
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
+                    if constexpr (LY::kRawBC) {
+                        // NS bf16 values = NS / 2 words per row, 8- or 16-byte loads
+                        const uint32_t *Bw = reinterpret_cast<const uint32_t *>(st + LY::s_B) +
+                                             ((tb + u) * N + j * NS) / 2;
+                        const uint32_t *Cw = reinterpret_cast<const uint32_t *>(st + LY::s_C) +
+                                             ((tb + u) * N + j * NS) / 2;
+                        constexpr int kW = (NS / 2) % 4 == 0 ? 4 : 2;
+#pragma unroll
+                        for (int k = 0; k < NS / 2; k += kW) {
+                            uint32_t wb[kW], wc[kW];
+                            if constexpr (kW == 4) {
+                                const uint4 b4 = *reinterpret_cast<const uint4 *>(Bw + k);
+                                wb[0] = b4.x; wb[1] = b4.y; wb[2] = b4.z; wb[3] = b4.w;
+                                if (!kSummary) {
+                                    const uint4 c4 = *reinterpret_cast<const uint4 *>(Cw + k);
+                                    wc[0] = c4.x; wc[1] = c4.y; wc[2] = c4.z; wc[3] = c4.w;
+                                }
+                            } else {
+                                const uint2 b2 = *reinterpret_cast<const uint2 *>(Bw + k);
+                                wb[0] = b2.x; wb[1] = b2.y;
+                                if (!kSummary) {
+                                    const uint2 c2 = *reinterpret_cast<const uint2 *>(Cw + k);
+                                    wc[0] = c2.x; wc[1] = c2.y;
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < kW; ++i) {
+                                bp[u][k + i] = ptx::bf2_to_f2(wb[i]);
+                                if (!kSummary) cp[u][k + i] = ptx::bf2_to_f2(wc[i]);
+                            }
+                        }
+                        continue;
+                    }
                     const float *Bt = Bf + (tb + u) * N + j * NS;
                     const float *Ct = Cf + (tb + u) * N + j * NS;
 #pragma unroll
