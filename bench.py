@@ -41,7 +41,10 @@ L2_FLUSH_BYTES = 256 << 20
 # ncu DRAM traffic (bytes) per launch of the dominant kernel, keyed by the sha256
 # prefix of the kernel's sources at the time of the capture; an entry whose key no
 # longer matches the sources is ignored (traffic reported as null).
-PROFILED_TRAFFIC = {}
+PROFILED_TRAFFIC = {
+    # scan_tma_kernel, 130M-layer workload: 152,191,744 B read + 31,835,648 B written
+    "277ca20cd6132540": 184027392,
+}
 
 WORKLOADS = {
     "scan_bf16_B8_D1536_L2048_N16": 1,
@@ -49,7 +52,7 @@ WORKLOADS = {
     "ssd_bf16_B4_L8192_H80_P64_N128_G1_Q256": 3,
     "decode_bf16_B256_D5120_N16_x1000": 4,
 }
-SCAN_SOURCES = ["scan_tma.cu", "scan_fwd.cu", "common.cuh", "ptx.cuh", "internal.h"]
+SCAN_SOURCES = ["scan_tma.cu", "scan_fwd.cu", "common.cuh", "ptx.cuh"]
 
 
 # ------------------------------------------------------------------ small helpers
@@ -284,6 +287,23 @@ def e2e_scan(p, steps, device):
     return s.elapsed_time(e) * 1e-3 / steps, h2d, d2h
 
 
+def _median_event_time(step, flush, iters):
+    import torch
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e-3)
+    return float(np.median(times))
+
+
 def time_ssd(p, iters, flush, device):
     import torch
     import selective_state_space_132_b300 as ssm
@@ -300,18 +320,7 @@ def time_ssd(p, iters, flush, device):
     def step():
         ssm.ssd_chunk_fwd(x, dl, A, Bm, Cm, D=Dv, delta_bias=bias, chunk_size=p.chunk, y=y,
                           h_final=hf, workspace=ws)
-    step()
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(iters):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        step()
-        b.record()
-        torch.cuda.synchronize()
-        times.append(a.elapsed_time(b) * 1e-3)
-    return float(np.median(times))
+    return _median_event_time(step, flush, iters)
 
 
 def time_decode(p, steps, flush, device, pool=8):
@@ -375,23 +384,6 @@ def time_ssd_decode(nb, H, P, G, N, flush, device, iters=30):
 
     def step():
         ssm.ssd_step_decode(state, x, dl, A, Bm, Cm, D=Dv, delta_bias=bias, y=y)
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(iters):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        step()
-        b.record()
-        torch.cuda.synchronize()
-        times.append(a.elapsed_time(b) * 1e-3)
-    return float(np.median(times))
-
-
-def _median_event_time(step, flush, iters):
-    import torch
     for _ in range(3):
         step()
     torch.cuda.synchronize()

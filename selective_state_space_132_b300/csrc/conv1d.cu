@@ -25,6 +25,7 @@ constexpr int kNB = 4;     // batches per thread
 constexpr int kT = kR * kNB;   // time steps per thread
 constexpr int kMaxK = 8;
 
+
 // Raw 16-byte (or one-element) rows and their widening to fp32.
 template <typename TIO, int VEC> struct Vec;
 template <> struct Vec<__nv_bfloat16, 8> {
