@@ -267,7 +267,10 @@ SSM_API ssm_status ssm_ssd_step_decode(const ssm_ssd_decode_args *args, ssm_stre
  * or is zero when x_prev is NULL, so a sequence can be processed in pieces.
  * Shapes: x, out (B, L, D) io_dtype; x_prev (B, K - 1, D) io_dtype; weight (D, K) fp32;
  * bias (D) fp32.  Nullable: bias, x_prev.  1 <= K <= 8; silu 0 returns the
- * convolution alone.  out may not alias x or x_prev.  No workspace. */
+ * convolution alone.  out may not alias x or x_prev.
+ * workspace (optional): a 256-byte device status word, read with
+ * ssm_read_device_status; the TMA-tiled kernel records SSM_ERR_TIMEOUT there if one of
+ * its bounded waits gives up (without a workspace such a timeout goes unreported). */
 typedef struct {
     int64_t batch, seqlen, dim, width;
     int32_t io_dtype;
@@ -275,6 +278,8 @@ typedef struct {
     const void *x, *x_prev;
     const float *weight, *bias;
     void *out;
+    void *workspace;           /* nullable; if given, >= 256 bytes, 256-byte aligned */
+    size_t workspace_bytes;
 } ssm_conv1d_args;
 
 SSM_API ssm_status ssm_conv1d(const ssm_conv1d_args *args, ssm_stream_t stream);

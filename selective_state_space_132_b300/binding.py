@@ -67,7 +67,8 @@ class ScanBwdArgs(ctypes.Structure):
 class Conv1dArgs(ctypes.Structure):
     _fields_ = [("batch", _i64), ("seqlen", _i64), ("dim", _i64), ("width", _i64),
                 ("io_dtype", _i32), ("silu", _i32), ("x", _vp), ("x_prev", _vp),
-                ("weight", _fp), ("bias", _fp), ("out", _vp)]
+                ("weight", _fp), ("bias", _fp), ("out", _vp), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 DISCRETIZATIONS = {"euler": 0, "zoh": 1}
@@ -498,10 +499,12 @@ def ssd_step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A
 # ---------------------------------------------------------------- causal conv1d + SiLU
 def conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
            x_prev: Optional[torch.Tensor] = None, silu: bool = True,
-           out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+           out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+           stream=None) -> torch.Tensor:
     """Causal depthwise convolution along time, then SiLU.  x: (B, L, D); weight: (D, K)
     fp32; bias: (D,) fp32; x_prev: (B, K-1, D), the inputs just before x (zeros when
-    None).  Returns (B, L, D) in x's dtype."""
+    None); workspace: optional 256-byte device status word (read_device_status).
+    Returns (B, L, D) in x's dtype."""
     lib = load_library()
     nb, L, Dm = x.shape
     K = weight.shape[1]
@@ -515,6 +518,7 @@ def conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] =
         out = torch.empty_like(x)
     _check(out, "out", (nb, L, Dm), io, dev)
     args = Conv1dArgs(nb, L, Dm, K, _io_code(x), int(bool(silu)), _ptr(x), _ptr(x_prev),
-                      _ptr(weight), _ptr(bias), _ptr(out))
+                      _ptr(weight), _ptr(bias), _ptr(out), _ptr(workspace),
+                      0 if workspace is None else workspace.numel() * workspace.element_size())
     _raise(lib.ssm_conv1d(ctypes.byref(args), _stream(stream)), "ssm_conv1d")
     return out

@@ -13,8 +13,14 @@
 // channels stay in registers.
 // Shapes whose rows cannot be split into aligned 16-byte chunks run one channel per
 // thread.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/ssm.h"
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace ssm {
 namespace {
@@ -157,6 +163,246 @@ __global__ void __launch_bounds__(kBlock) conv1d_kernel(Conv1dParams p) {
     }
 }
 
+// ---------------------------------------------------------------- TMA-tiled kernel
+// Persistent blocks walk tiles of TT = 128 steps x one 128-byte row of channels (64 bf16
+// or 32 fp32) of one batch row.  A block takes a contiguous range of tiles in
+// channel-slab-major order, so its taps change only at a slab boundary and consecutive
+// tiles are consecutive time strips.  A three-stage TMA pipeline brings each tile with
+// its K - 1 halo rows: the box starts K - 1 steps before the tile, and rows before t = 0
+// are zero-filled by the TMA unit (or taken from x_prev).  Each thread computes
+// RPT = 4 consecutive rows of one 16-byte chunk from shared memory; the outputs go to a
+// double-buffered shared tile that one TMA store writes back.  The rows never pass
+// through the LSU queue of a thread, and the thread body is small.
+constexpr int kBlockT = 256;
+constexpr int kTT = 128;           // steps per tile
+constexpr int kStagesT = 3;
+constexpr int kRowB = 128;         // bytes of channels per tile row
+constexpr int kStageB = ((kTT + kMaxK - 1) * kRowB + 1023) / 1024 * 1024;
+constexpr int kYB = kTT * kRowB;
+constexpr int kOffY = kStagesT * kStageB;
+constexpr int kOffBar = kOffY + 2 * kYB;
+constexpr int kTmaSmem = kOffBar + kStagesT * 8 + 1024;   // + slack to align the base
+
+struct Conv1dMaps {
+    CUtensorMap x, y;
+};
+
+template <typename TIO, int K, bool kFast>
+__global__ void __launch_bounds__(kBlockT) conv1d_tma_kernel(const __grid_constant__ Conv1dMaps maps,
+                                                             const Conv1dParams p) {
+    using V = Vec<TIO, 16 / sizeof(TIO)>;
+    constexpr int VEC = 16 / sizeof(TIO);
+    constexpr int TD = kRowB / sizeof(TIO);     // channels per tile
+    constexpr int CH = kRowB / 16;              // 16-byte chunks per row (8)
+    constexpr int RPT = kTT * CH / kBlockT;     // rows per thread (4)
+    constexpr uint32_t kTx = (kTT + K - 1) * kRowB;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
+
+    const int tid = threadIdx.x;
+    const int q = tid % CH, rg = tid / CH;
+    const int64_t D = p.dim, L = p.seqlen;
+    const int64_t nds = (D + TD - 1) / TD, nts = (L + kTT - 1) / kTT;
+    const int64_t nstrips = p.batch * nts;
+    const int64_t ntiles = nds * nstrips;
+    // this block's contiguous range [k0, k1) of tiles
+    const int64_t G = gridDim.x, per = ntiles / G, rem = ntiles % G;
+    const int64_t k0 = blockIdx.x * per + (blockIdx.x < rem ? blockIdx.x : rem);
+    const int64_t k1 = k0 + per + (blockIdx.x < rem ? 1 : 0);
+    auto coords = [&](int64_t k, int &d0, int &t0, int &b) {
+        d0 = static_cast<int>((k / nstrips) * TD);
+        const int64_t strip = k % nstrips;
+        b = static_cast<int>(strip / nts);
+        t0 = static_cast<int>((strip % nts) * kTT);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStagesT; ++s) ptx::mbar_init(&bars[s], 1);
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&maps.x);
+        ptx::prefetch_tmap(&maps.y);
+        for (int s = 0; s < kStagesT && k0 + s < k1; ++s) {
+            int d0, t0, b;
+            coords(k0 + s, d0, t0, b);
+            ptx::mbar_arrive_expect_tx(&bars[s], kTx);
+            ptx::tma_load_3d(smem + s * kStageB, &maps.x, &bars[s], d0, t0 - (K - 1), b);
+        }
+    }
+    __syncthreads();
+
+    const TIO *gprev = static_cast<const TIO *>(p.x_prev);
+    float wf[VEC * K], bias[VEC];
+    int cur_d0 = -1;
+    bool cin = false;
+    int64_t failed = -1;
+    for (int64_t k = k0; k < k1; ++k) {
+        const int it = static_cast<int>(k - k0);
+        const int s = it % kStagesT;
+        // the y buffer of this tile was last stored two tiles ago
+        if (tid == 0) ptx::bulk_wait_read<1>();
+        const bool got = ptx::mbar_wait(&bars[s], (it / kStagesT) & 1);
+        if (!__syncthreads_and(got ? 1 : 0)) {
+            failed = k;
+            break;
+        }
+        int d0, t0, b;
+        coords(k, d0, t0, b);
+        const int dq = d0 + q * VEC;            // first channel of this thread's chunk
+        if (d0 != cur_d0) {
+            // the taps of the chunk's VEC channels are VEC * K consecutive floats
+            // (16-byte aligned: dq is a multiple of VEC); D is a multiple of VEC, so a
+            // chunk is either wholly inside the tensor or wholly past it
+            cur_d0 = d0;
+            cin = dq < D;
+#pragma unroll
+            for (int i = 0; i < VEC * K / 4; ++i) {
+                const float4 v = cin ? __ldg(reinterpret_cast<const float4 *>(p.weight + dq * K) + i)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                wf[4 * i] = v.x; wf[4 * i + 1] = v.y; wf[4 * i + 2] = v.z; wf[4 * i + 3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < VEC / 4; ++i) {
+                const float4 v = (cin && p.bias)
+                                     ? __ldg(reinterpret_cast<const float4 *>(p.bias + dq) + i)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                bias[4 * i] = v.x; bias[4 * i + 1] = v.y; bias[4 * i + 2] = v.z;
+                bias[4 * i + 3] = v.w;
+            }
+        }
+        const unsigned char *st = smem + s * kStageB;
+        unsigned char *yb = smem + kOffY + (it & 1) * kYB;
+        // stage row j holds step t0 - (K - 1) + j; output row r needs stage rows r .. r + K - 1
+        auto row = [&](int j, float (&v)[VEC]) {
+            const int t = t0 - (K - 1) + j;
+            if (t < 0 && gprev && cin) {
+                V::widen(V::load(gprev + (static_cast<int64_t>(b) * (K - 1) + (K - 1 + t)) * D + dq), v);
+            } else {
+                V::widen(*reinterpret_cast<const typename V::Raw *>(st + j * kRowB + q * 16), v);
+            }
+        };
+        float win[K][VEC];
+#pragma unroll
+        for (int kk = 0; kk < K - 1; ++kk) row(rg * RPT + kk, win[kk]);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int orow = rg * RPT + r;
+            row(orow + K - 1, win[K - 1]);
+            float out[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                float acc = bias[e];
+#pragma unroll
+                for (int kk = 0; kk < K; ++kk) acc = fmaf(wf[e * K + kk], win[kk][e], acc);
+                out[e] = p.silu ? silu<kFast>(acc) : acc;
+            }
+            V::store(reinterpret_cast<TIO *>(yb + orow * kRowB + q * 16), out);
+#pragma unroll
+            for (int kk = 0; kk < K - 1; ++kk)
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) win[kk][e] = win[kk + 1][e];
+        }
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            ptx::tma_store_3d(&maps.y, yb, d0, t0, b);
+            ptx::bulk_commit();
+            if (k + kStagesT < k1) {
+                int nd0, nt0, nb;
+                coords(k + kStagesT, nd0, nt0, nb);
+                ptx::mbar_arrive_expect_tx(&bars[s], kTx);
+                ptx::tma_load_3d(smem + s * kStageB, &maps.x, &bars[s], nd0, nt0 - (K - 1), nb);
+            }
+        }
+    }
+    if (failed >= 0) {
+        if (tid == 0) {
+            report_status(status, SSM_ERR_TIMEOUT, 40);
+            // give every load still in flight one more bounded wait before the shared
+            // memory is released
+            for (int64_t j = failed; j < failed + kStagesT && j < k1; ++j) {
+                const int jt = static_cast<int>(j - k0);
+                (void)ptx::mbar_wait(&bars[jt % kStagesT], (jt / kStagesT) & 1);
+            }
+        }
+        __syncthreads();
+    }
+    if (tid == 0) ptx::bulk_wait<0>();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult qr{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// (B, L, D) row-major tensor, box (one 128-byte row of channels, rows, 1), no swizzle.
+bool conv_map(CUtensorMap *m, const void *base, bool bf16, int64_t B, int64_t L, int64_t D,
+              int rows) {
+    auto enc = tma_encoder();
+    if (!enc) return false;
+    const size_t e = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * e), static_cast<cuuint64_t>(L * D * e)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kRowB / e), static_cast<cuuint32_t>(rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename TIO, int K>
+cudaError_t launch_tma_k(const Conv1dParams &p, cudaStream_t stream) {
+    constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
+    constexpr int TD = kRowB / sizeof(TIO);
+    Conv1dMaps m;
+    const bool bf = sizeof(TIO) == 2;
+    if (!conv_map(&m.x, p.x, bf, p.batch, p.seqlen, p.dim, kTT + K - 1) ||
+        !conv_map(&m.y, p.out, bf, p.batch, p.seqlen, p.dim, kTT))
+        return cudaErrorInvalidValue;
+    auto kern = conv1d_tma_kernel<TIO, K, kFast>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTmaSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    const int64_t ntiles = p.batch * ((p.seqlen + kTT - 1) / kTT) * ((p.dim + TD - 1) / TD);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBlockT, kTmaSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * (per_sm > 0 ? per_sm : 1);
+    const unsigned grid = static_cast<unsigned>(ntiles < cap ? ntiles : cap);
+    kern<<<grid, kBlockT, kTmaSmem, stream>>>(m, p);
+    return cudaGetLastError();
+}
+
+template <typename TIO> cudaError_t launch_tma(const Conv1dParams &p, cudaStream_t st) {
+    switch (p.width) {
+        case 1: return launch_tma_k<TIO, 1>(p, st);
+        case 2: return launch_tma_k<TIO, 2>(p, st);
+        case 3: return launch_tma_k<TIO, 3>(p, st);
+        case 4: return launch_tma_k<TIO, 4>(p, st);
+        case 5: return launch_tma_k<TIO, 5>(p, st);
+        case 6: return launch_tma_k<TIO, 6>(p, st);
+        case 7: return launch_tma_k<TIO, 7>(p, st);
+        case 8: return launch_tma_k<TIO, 8>(p, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <typename TIO, int VEC, int K>
 cudaError_t launch_k(const Conv1dParams &p, cudaStream_t stream) {
     constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
@@ -182,6 +428,7 @@ template <typename TIO, int VEC> cudaError_t launch_vec(const Conv1dParams &p, c
 
 template <typename TIO> cudaError_t launch_typed(const Conv1dParams &p, cudaStream_t stream) {
     constexpr int kVec = 16 / sizeof(TIO);
+    if (conv1d_tma_ok(p)) return launch_tma<TIO>(p, stream);
     const bool vec = p.dim % kVec == 0 &&
                      reinterpret_cast<uintptr_t>(p.x) % 16 == 0 &&
                      reinterpret_cast<uintptr_t>(p.out) % 16 == 0 &&
@@ -192,6 +439,14 @@ template <typename TIO> cudaError_t launch_typed(const Conv1dParams &p, cudaStre
 }  // namespace
 
 int conv1d_max_width() { return kMaxK; }
+
+bool conv1d_tma_ok(const Conv1dParams &p) {
+    const size_t e = p.io_bf16 ? 2 : 4;
+    auto a16 = [](const void *q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+    return (p.dim * e) % 16 == 0 && a16(p.x) && a16(p.out) && a16(p.x_prev) && a16(p.weight) &&
+           a16(p.bias) && p.seqlen < (int64_t(1) << 31) &&
+           p.batch < (int64_t(1) << 31) && p.dim < (int64_t(1) << 31) && tma_encoder() != nullptr;
+}
 
 cudaError_t launch_conv1d(const Conv1dParams &p, cudaStream_t stream) {
     return p.io_bf16 ? launch_typed<__nv_bfloat16>(p, stream) : launch_typed<float>(p, stream);

@@ -103,8 +103,10 @@ struct Conv1dParams {
     const void *x, *x_prev;
     const float *weight, *bias;
     void *out;
+    void *status;   // device status word (nullable)
 };
 int conv1d_max_width();
+bool conv1d_tma_ok(const Conv1dParams &p);
 cudaError_t launch_conv1d(const Conv1dParams &p, cudaStream_t stream);
 
 }  // namespace ssm

@@ -265,6 +265,10 @@ ssm_status check_conv1d(const ssm_conv1d_args *a) {
     const size_t prev = (size_t)(a->batch * (a->width - 1) * a->dim) * e;
     if (overlaps(a->out, tok, a->x, tok) || overlaps(a->out, tok, a->x_prev, prev))
         return SSM_ERR_INVALID_ARG;
+    if (a->workspace) {
+        if (a->workspace_bytes < ssm::kStatusBytes) return SSM_ERR_WORKSPACE;
+        if (!aligned(a->workspace, 256)) return SSM_ERR_ALIGNMENT;
+    }
     return SSM_OK;
 }
 
@@ -526,7 +530,11 @@ ssm_status ssm_conv1d(const ssm_conv1d_args *a, ssm_stream_t stream) {
     p.weight = a->weight;
     p.bias = a->bias;
     p.out = a->out;
-    return from_cuda(ssm::launch_conv1d(p, reinterpret_cast<cudaStream_t>(stream)));
+    p.status = a->workspace;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (a->workspace && cudaMemsetAsync(a->workspace, 0, ssm::kStatusBytes, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return from_cuda(ssm::launch_conv1d(p, st));
 }
 
 ssm_status ssm_read_device_status(const void *workspace, ssm_stream_t stream,

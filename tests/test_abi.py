@@ -257,6 +257,8 @@ def test_conv1d_rejects_bad_arguments(lib):
     assert rc(weight=0x200002) == ALIGN
     assert rc(out=0x100000) == INVALID               # out aliases x
     assert rc(out=0x400000, x_prev=0x400010) == INVALID   # out overlaps x_prev
+    assert rc(workspace=0xc00000, workspace_bytes=128) == WORKSPACE   # status word is 256 B
+    assert rc(workspace=0xc00010, workspace_bytes=256) == ALIGN
     assert rc(seqlen=0) == OK                        # nothing to do, nothing launched
 
 

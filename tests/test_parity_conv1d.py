@@ -92,3 +92,17 @@ def test_conv1d_block_shape_sampled():
     rows = [0, 3, 7]
     ref = oracle.conv1d(_round(x[rows], "bf16"), w.astype(np.float32), b.astype(np.float32))
     assert_close(out[rows], ref, "bf16", "sampled rows")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_conv1d_status_word_stays_clear(io):
+    """With a status workspace the TMA-tiled kernel leaves SSM_OK there."""
+    x, w, b, xp = _inputs(2, 300, 128, 4, seed=12, prev=True)
+    t = io_dtype(io)
+    ws = torch.full((256,), 7, dtype=torch.uint8, device="cuda")
+    out = ssm.conv1d(dev(x, t), dev(w), dev(b), x_prev=dev(xp, t), workspace=ws)
+    torch.cuda.synchronize()
+    assert ssm.read_device_status(ws) == 0
+    ref = oracle.conv1d(_round(x, io), w.astype(np.float32), b.astype(np.float32),
+                        x_prev=_round(xp, io))
+    assert_close(host(out), ref, io, "conv1d with carried window")
