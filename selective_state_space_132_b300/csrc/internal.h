@@ -27,7 +27,7 @@ struct ScanParams {
 
 // TMA-staged scan (scan_tma.cu): warps per 32-channel block for these sizes (0 = the
 // sizes are not supported), whether a call can take it, and the launch.
-int scan_tma_block_warps(int io_bf16, int64_t dstate);
+int scan_tma_blocks_per_sm(int io_bf16, int64_t dstate);
 bool scan_tma_sizes_ok(int io_bf16, int64_t seqlen, int64_t dim, int64_t dstate);
 bool scan_tma_pointers_ok(const void *const *ptrs, int nptrs);
 int device_sm_count();
@@ -36,7 +36,7 @@ cudaError_t launch_scan_tma(const ScanParams &p, cudaStream_t stream);
 // Number of time chunks and chunk length the scan uses for these sizes; `tma_warps` > 0
 // selects the plan of the TMA-staged path (blocks of 32 channels and that many warps).
 void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t time_chunk,
-               int tma_warps, int64_t *chunk_len, int *nchunks);
+               int tma_blocks_per_sm, int64_t *chunk_len, int *nchunks);
 size_t scan_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, int nchunks);
 cudaError_t launch_scan(const ScanParams &p, cudaStream_t stream);
 

@@ -39,7 +39,6 @@ namespace ssm {
 namespace {
 
 constexpr int kTT = 32;  // time steps per shared-memory tile
-constexpr int kTmaWarpsPerSm = 8;
 constexpr int kDT = 32;  // channels per thread block
 constexpr int kRowF = kTT + 4;  // floats per per-channel row (16-byte aligned, conflict-free)
 
@@ -359,23 +358,29 @@ int device_sm_count() {
 }
 
 void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t time_chunk,
-               int tma_warps, int64_t *chunk_len, int *nchunks) {
+               int tma_blocks_per_sm, int64_t *chunk_len, int *nchunks) {
     int64_t cl;
     if (time_chunk > 0) {
         cl = (time_chunk + kTT - 1) / kTT * kTT;
     } else {
-        // Enough warps to keep every SM busy, about eight deep.  Each extra chunk costs a
-        // summary pass over that chunk (most of a scan of it), so split only when short
-        // of it and keep chunks at least 1024 steps long.
-        int64_t warps, target;
-        if (tma_warps > 0) {
-            warps = batch * ((dim + 31) / 32) * tma_warps;
-            target = static_cast<int64_t>(device_sm_count()) * kTmaWarpsPerSm;
+        // Each extra chunk costs a summary pass over that chunk (most of a scan of it),
+        // so the sequence is split only when its chains alone cannot fill the GPU.
+        //  * TMA kernel: the largest split whose grid still fits in one wave of
+        //    resident blocks (measured on the long-context shape: 5 chunks 3.74 ms,
+        //    9 chunks (one full wave) 2.86 ms, 12 chunks (1.3 waves) 3.03 ms); the
+        //    130M-layer shape (384 blocks, 592 slots) stays whole.
+        //  * general kernel: about eight warps per SM.
+        // Chunks stay at least 1024 steps long.
+        int64_t k;
+        if (tma_blocks_per_sm > 0) {
+            const int64_t per_chunk = batch * ((dim + 31) / 32);
+            const int64_t slots = static_cast<int64_t>(device_sm_count()) * tma_blocks_per_sm;
+            k = per_chunk > 0 ? slots / per_chunk : 1;
         } else {
-            warps = batch * ((dim + kDT - 1) / kDT) * lanes_for(dstate);
-            target = static_cast<int64_t>(device_sm_count()) * 8;
+            const int64_t warps = batch * ((dim + kDT - 1) / kDT) * lanes_for(dstate);
+            const int64_t target = static_cast<int64_t>(device_sm_count()) * 8;
+            k = warps > 0 ? (target + warps - 1) / warps : 1;
         }
-        int64_t k = warps > 0 ? (target + warps - 1) / warps : 1;
         const int64_t kmax = std::max<int64_t>(1, seqlen / 1024);
         k = std::max<int64_t>(1, std::min(k, kmax));
         cl = (seqlen + k - 1) / k;

@@ -572,7 +572,37 @@ static int scan_tma_lpc(int io_bf16, int64_t dstate) {
     }
 }
 
-int scan_tma_block_warps(int io_bf16, int64_t dstate) { return scan_tma_lpc(io_bf16, dstate); }
+namespace {
+// Resident blocks per SM of the output kernel, from its shared memory (228 KiB per SM,
+// 1 KiB reserved per block) and its warps (64 per SM).
+template <typename TIO, int NS, int LPC> int blocks_per_sm() {
+    using LY = Layout<TIO, NS, LPC, LPC, false>;
+    const int by_smem = (228 * 1024) / (LY::bytes + 1024);
+    const int by_warps = 64 / LPC;
+    const int b = by_smem < by_warps ? by_smem : by_warps;
+    return b > 0 ? b : 1;
+}
+}  // namespace
+
+int scan_tma_blocks_per_sm(int io_bf16, int64_t dstate) {
+    if (io_bf16) {
+        switch (dstate) {
+            case 8: return blocks_per_sm<__nv_bfloat16, 4, 2>();
+            case 16: return blocks_per_sm<__nv_bfloat16, 4, 4>();
+            case 32: return blocks_per_sm<__nv_bfloat16, 8, 4>();
+            case 64: return blocks_per_sm<__nv_bfloat16, 16, 4>();
+            default: return 0;
+        }
+    }
+    switch (dstate) {
+        case 4: return blocks_per_sm<float, 2, 2>();
+        case 8: return blocks_per_sm<float, 4, 2>();
+        case 16: return blocks_per_sm<float, 4, 4>();
+        case 32: return blocks_per_sm<float, 8, 4>();
+        case 64: return blocks_per_sm<float, 16, 4>();
+        default: return 0;
+    }
+}
 
 bool scan_tma_sizes_ok(int io_bf16, int64_t seqlen, int64_t dim, int64_t dstate) {
     const int64_t e = io_bf16 ? 2 : 4;

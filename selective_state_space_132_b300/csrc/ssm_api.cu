@@ -69,10 +69,10 @@ ssm_status check_scan(const ssm_scan_args *a, bool pointers = true) {
 // kernel on the same plan).  The workspace always holds the device status word.
 size_t scan_ws(const ssm_scan_args *a, int64_t *chunk_len, int *nchunks) {
     const int bf = a->io_dtype == SSM_BF16;
-    const int tma_warps = ssm::scan_tma_sizes_ok(bf, a->seqlen, a->dim, a->dstate)
-                              ? ssm::scan_tma_block_warps(bf, a->dstate)
-                              : 0;
-    ssm::scan_plan(a->batch, a->seqlen, a->dim, a->dstate, a->time_chunk, tma_warps, chunk_len,
+    const int tma_bps = ssm::scan_tma_sizes_ok(bf, a->seqlen, a->dim, a->dstate)
+                            ? ssm::scan_tma_blocks_per_sm(bf, a->dstate)
+                            : 0;
+    ssm::scan_plan(a->batch, a->seqlen, a->dim, a->dstate, a->time_chunk, tma_bps, chunk_len,
                    nchunks);
     return ssm::scan_workspace_bytes(a->batch, a->dim, a->dstate, *nchunks);
 }
