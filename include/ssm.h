@@ -62,7 +62,7 @@ typedef struct CUstream_st *ssm_stream_t;
 typedef enum {
     SSM_OK = 0,
     SSM_ERR_INVALID_ARG = 1, /* a null required pointer, a negative size, H % G != 0, ... */
-    SSM_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement (e.g. N > 64) */
+    SSM_ERR_UNSUPPORTED = 2, /* a valid request the library does not implement (e.g. N > 64) */
     SSM_ERR_ALIGNMENT = 3,   /* a pointer is not aligned to its element size */
     SSM_ERR_WORKSPACE = 4,   /* workspace missing or smaller than *_workspace_size says */
     SSM_ERR_CUDA = 5,        /* the CUDA runtime reported an error at launch */
