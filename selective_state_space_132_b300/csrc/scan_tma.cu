@@ -160,7 +160,6 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
     constexpr int EC = CK::EC;                  // elements per 16-byte chunk
     constexpr int QW = CPW / EC;                // chunks of a warp's channels in one row
     constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
-    constexpr int NT = 32 * WPC;
     static_assert(NS % 2 == 0 && CPW % EC == 0, "layout");
     static_assert(ROWB == 32 || ROWB == 64 || ROWB == 128, "token rows must match a TMA swizzle");
 

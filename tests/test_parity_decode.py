@@ -85,3 +85,11 @@ def test_decode_zero_order_hold(io):
                                 z=tok["z"], bias=p.bias, zoh=True)
         assert_close(host(y), yr, p.io, f"y step {s}")
     assert_close(host(state), ref, p.io, "state")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_decode_four_rows_per_thread_ragged_batch(io):
+    """Enough rows for the kernel to give each thread four batch rows of its channel;
+    130 rows leave a ragged last group of two."""
+    p = W.decode_problem(130, 1024, 16, 3, io=io, seed=160)
+    _decode_run(p, 3, rows=[0, 1, 2, 3, 64, 127, 128, 129])
