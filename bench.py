@@ -53,7 +53,7 @@ WORKLOADS = {
     "ssd_bf16_B4_L8192_H80_P64_N128_G1_Q256": 3,
     "decode_bf16_B256_D5120_N16_x1000": 4,
 }
-SCAN_SOURCES = ["scan_tma.cu", "scan_fwd.cu", "common.cuh", "ptx.cuh"]
+SCAN_SOURCES = ["scan_tma.cu", "scan_fwd.cu", "common.cuh", "ptx.cuh", "tma_host.cuh"]
 
 
 # ------------------------------------------------------------------ small helpers

@@ -15,12 +15,11 @@
 // thread.
 #include <cudaTypedefs.h>
 
-#include <mutex>
-
 #include "../../include/ssm.h"
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "tma_host.cuh"
 
 namespace ssm {
 namespace {
@@ -332,45 +331,15 @@ __global__ void __launch_bounds__(kBlockT) conv1d_tma_kernel(const __grid_consta
     if (tid == 0) ptx::bulk_wait<0>();
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult qr{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                             cudaEnableDefault, &qr) == cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// (B, L, D) row-major tensor, box (one 128-byte row of channels, rows, 1), no swizzle.
-bool conv_map(CUtensorMap *m, const void *base, bool bf16, int64_t B, int64_t L, int64_t D,
-              int rows) {
-    auto enc = tma_encoder();
-    if (!enc) return false;
-    const size_t e = bf16 ? 2 : 4;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
-                          static_cast<cuuint64_t>(B)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * e), static_cast<cuuint64_t>(L * D * e)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(kRowB / e), static_cast<cuuint32_t>(rows), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename TIO, int K>
 cudaError_t launch_tma_k(const Conv1dParams &p, cudaStream_t stream) {
     constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
     constexpr int TD = kRowB / sizeof(TIO);
     Conv1dMaps m;
     const bool bf = sizeof(TIO) == 2;
-    if (!conv_map(&m.x, p.x, bf, p.batch, p.seqlen, p.dim, kTT + K - 1) ||
-        !conv_map(&m.y, p.out, bf, p.batch, p.seqlen, p.dim, kTT))
+    constexpr int kRowE = kRowB / static_cast<int>(sizeof(TIO));   // channels per tile row
+    if (!make_tma_map_3d(&m.x, p.x, bf, p.batch, p.seqlen, p.dim, kRowE, kTT + K - 1, 0) ||
+        !make_tma_map_3d(&m.y, p.out, bf, p.batch, p.seqlen, p.dim, kRowE, kTT, 0))
         return cudaErrorInvalidValue;
     auto kern = conv1d_tma_kernel<TIO, K, kFast>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

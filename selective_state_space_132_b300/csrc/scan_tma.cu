@@ -40,11 +40,10 @@
 
 #include "../../include/ssm.h"
 
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "tma_host.cuh"
 
 namespace ssm {
 namespace {
@@ -478,43 +477,6 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// 3-D map over a (B, L, W) row-major tensor, box (bw, bt, 1); `swizzle_bytes` 0, 32,
-// 64 or 128 selects the shared-memory swizzle of the box rows.
-bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t B, int64_t L, int64_t W,
-              int bw, int bt, int swizzle_bytes) {
-    auto enc = encoder();
-    if (!enc) return false;
-    const size_t e = bf16 ? 2 : 4;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(L),
-                          static_cast<cuuint64_t>(B)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(W * e), static_cast<cuuint64_t>(L * W * e)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(bw), static_cast<cuuint32_t>(bt), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
-                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                  : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
-                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
-    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                     3, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh>
 cudaError_t launch_tma_one(const ScanParams &p, const TmaMaps &maps, int nchunks_grid,
                            cudaStream_t stream) {
@@ -539,12 +501,12 @@ cudaError_t launch_tma_pair(ScanParams p, cudaStream_t stream) {
     const bool bf = std::is_same<TIO, __nv_bfloat16>::value;
     TmaMaps m{};
     const int64_t B = p.batch, L = p.seqlen, D = p.dim, N = p.dstate;
-    bool ok = make_map(&m.x, p.x, bf, B, L, D, LY::CPB, kT, LY::ROWB) &&
-              make_map(&m.dl, p.delta, bf, B, L, D, LY::CPB, kT, LY::ROWB) &&
-              make_map(&m.B, p.Bm, bf, B, L, N, static_cast<int>(N), kT, 0) &&
-              make_map(&m.C, p.Cm, bf, B, L, N, static_cast<int>(N), kT, 0) &&
-              make_map(&m.y, p.y, bf, B, L, D, LY::CPB, kT, LY::ROWB);
-    if (ok && p.z) ok = make_map(&m.z, p.z, bf, B, L, D, LY::CPB, kT, LY::ROWB);
+    bool ok = make_tma_map_3d(&m.x, p.x, bf, B, L, D, LY::CPB, kT, LY::ROWB) &&
+              make_tma_map_3d(&m.dl, p.delta, bf, B, L, D, LY::CPB, kT, LY::ROWB) &&
+              make_tma_map_3d(&m.B, p.Bm, bf, B, L, N, static_cast<int>(N), kT, 0) &&
+              make_tma_map_3d(&m.C, p.Cm, bf, B, L, N, static_cast<int>(N), kT, 0) &&
+              make_tma_map_3d(&m.y, p.y, bf, B, L, D, LY::CPB, kT, LY::ROWB);
+    if (ok && p.z) ok = make_tma_map_3d(&m.z, p.z, bf, B, L, D, LY::CPB, kT, LY::ROWB);
     if (!ok) return cudaErrorInvalidValue;
     p.clear_status = 1;
     if (p.nchunks > 1) {
@@ -613,7 +575,7 @@ bool scan_tma_sizes_ok(int io_bf16, int64_t seqlen, int64_t dim, int64_t dstate)
 bool scan_tma_pointers_ok(const void *const *ptrs, int nptrs) {
     for (int i = 0; i < nptrs; ++i)
         if (ptrs[i] && reinterpret_cast<uintptr_t>(ptrs[i]) % 16 != 0) return false;
-    return encoder() != nullptr;
+    return tma_encoder() != nullptr;
 }
 
 template <bool kZoh> cudaError_t launch_scan_tma_disc(const ScanParams &p, cudaStream_t stream) {

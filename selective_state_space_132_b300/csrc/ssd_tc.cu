@@ -49,6 +49,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "tma_host.cuh"
 
 namespace ssm {
 namespace {
@@ -507,36 +508,6 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-    return fn;
-}
-
-// 3-D bf16 map over a (B, L, W) row-major tensor, box (64, 128, 1), 128-byte swizzle.
-bool make_map_sw128(CUtensorMap *m, const void *base, int64_t B, int64_t L, int64_t W) {
-    auto enc = encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(L),
-                          static_cast<cuuint64_t>(B)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(W * 2), static_cast<cuuint64_t>(L * W * 2)};
-    cuuint32_t box[3] = {64, kQ, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool ssd_tc_sizes_ok(const SSDParams &p) {
@@ -550,7 +521,7 @@ bool ssd_tc_eligible(const SSDParams &p) {
     const void *ptrs[] = {p.x, p.Bm, p.Cm, p.z, p.y};
     for (const void *q : ptrs)
         if (q && reinterpret_cast<uintptr_t>(q) % 16 != 0) return false;
-    return encoder() != nullptr;
+    return tma_encoder() != nullptr;
 }
 
 // Persistent grid: two blocks per SM (their TMEM and shared memory fill an SM), but
@@ -580,9 +551,12 @@ size_t ssd_clear_bytes(const SSDParams &p) {
 cudaError_t launch_ssd_tc(const SSDParams &p, cudaStream_t stream) {
     Maps m{};
     const int64_t B = p.batch, L = p.seqlen, H = p.nheads, G = p.ngroups;
-    bool ok = make_map_sw128(&m.C, p.Cm, B, L, G * kN) && make_map_sw128(&m.B, p.Bm, B, L, G * kN) &&
-              make_map_sw128(&m.X, p.x, B, L, H * kP) && make_map_sw128(&m.Y, p.y, B, L, H * kP);
-    if (ok && p.z) ok = make_map_sw128(&m.Z, p.z, B, L, H * kP);
+    // bf16 boxes of 64 columns x 128 steps, 128-byte swizzle (the UMMA operand layout)
+    bool ok = make_tma_map_3d(&m.C, p.Cm, true, B, L, G * kN, 64, kQ, 128) &&
+              make_tma_map_3d(&m.B, p.Bm, true, B, L, G * kN, 64, kQ, 128) &&
+              make_tma_map_3d(&m.X, p.x, true, B, L, H * kP, 64, kQ, 128) &&
+              make_tma_map_3d(&m.Y, p.y, true, B, L, H * kP, 64, kQ, 128);
+    if (ok && p.z) ok = make_tma_map_3d(&m.Z, p.z, true, B, L, H * kP, 64, kQ, 128);
     if (!ok) return cudaErrorInvalidValue;
     Split sk{};
     sk.nch = static_cast<int>((L + kQ - 1) / kQ);
