@@ -13,7 +13,7 @@ from _parity import TOL, assert_close, dev, host, io_dtype, run_scan, run_ssd
 
 pytestmark = pytest.mark.gpu
 
-CASES = 12
+CASES = 24
 
 
 def _positive_steps(p, io, rng):
@@ -135,3 +135,28 @@ def test_random_decode_steps(case):
         torch.cuda.synchronize()
         assert_close(host(y), yr, io, f"decode y step {s} (B {nb} D {D} N {N})")
     assert_close(host(state), ref, io, "decode state")
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_random_ssd_decode_steps(case):
+    rng = np.random.default_rng(1500 + case)
+    io = ("f32", "bf16")[case % 2]
+    nb = int(rng.integers(1, 6))
+    G = int(rng.choice([1, 2]))
+    H = G * int(rng.integers(1, 5))
+    P = int(rng.choice([1, 3, 16, 64]))
+    N = int(rng.choice([5, 8, 16, 40, 64, 128, 200]))
+    p = W.ssd_problem(nb, 3, H, P, G, N, io=io, seed=1600 + case, gate=bool(case % 3), h0=True)
+    iot = io_dtype(io)
+    state = dev(p.h0)
+    ref = p.h0.astype(np.float64).copy()
+    for s in range(3):
+        y = ssm.ssd_step_decode(state, dev(p.x[:, s], iot), dev(p.delta[:, s], iot), dev(p.A),
+                                dev(p.B[:, s], iot), dev(p.C[:, s], iot), D=dev(p.D),
+                                z=None if p.z is None else dev(p.z[:, s], iot),
+                                delta_bias=dev(p.bias))
+        yr = oracle.ssd_decode_step(ref, p.x[:, s], p.delta[:, s], p.A, p.B[:, s], p.C[:, s],
+                                    Dv=p.D, z=None if p.z is None else p.z[:, s], bias=p.bias)
+        torch.cuda.synchronize()
+        assert_close(host(y), yr, io, f"ssd decode y step {s} (B {nb} H {H} P {P} G {G} N {N})")
+    assert_close(host(state), ref, io, "ssd decode state")
