@@ -76,6 +76,30 @@ def kernel_source_hash(names):
     return h.hexdigest()[:16]
 
 
+# Per-SM issue rates measured on B300 with a throughput microbenchmark (lanes per clock)
+MUFU_EX2_PER_CLK = 29.7
+FFMA_PER_CLK = 113.0
+
+
+def scan_ceilings(p, algo_bytes, hbm_gbs, device):
+    """Lower bounds on one scan step from each unit, at the SM clock of the part:
+    MUFU (one exp per state update, plus softplus (2) and SiLU (1) per (t, d)), fp32
+    (four operations per update: dl*A, dl*x*B, the state FMA, the C readout FMA) and
+    HBM (the algorithmic bytes at the measured copy bandwidth)."""
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    sms = props.multi_processor_count
+    clk = 2032e6                      # maximum SM clock of the part (Hz)
+    units = p.updates
+    rows = p.batch * p.seqlen * p.dim
+    mufu = (units + 3 * rows) / (sms * MUFU_EX2_PER_CLK * clk)
+    fp32 = 4 * units / (sms * FFMA_PER_CLK * clk)
+    hbm = algo_bytes / (hbm_gbs * 1e9)
+    return {"mufu_us": mufu * 1e6, "fp32_us": fp32 * 1e6, "hbm_us": hbm * 1e6, "sms": sms,
+            "basis": "per-SM rates measured on B300: ex2 29.7 lanes/clk, FFMA 113/clk; "
+                     "2032 MHz"}
+
+
 def scan_bytes(nb, L, D, N, e, gate=True, h0=False):
     """Algorithmic bytes of one scan: x, delta (, z), y in the I/O dtype, B and C,
     A, D and the bias in fp32, the final state (and h0) in fp32; no h_t."""
@@ -563,6 +587,7 @@ def run_ours(args, world, rank, local):
                      "frac_of_nominal_8000": achieved / 8000.0, "source_hash": src_hash},
         "gpu_launches": launches * args.steps,
         "wall_ms_per_step_incl_flush": wall / args.steps * 1e3,
+        "ceilings": scan_ceilings(p, algo, hbm, device),
     }
     # end to end on every rank at once (each with its own pinned host buffers): the
     # job's updates over the slowest rank's time
