@@ -1,6 +1,7 @@
 // C ABI of libssm.so: host-side validation, workspace sizing and dispatch to the
 // kernels.  Every check runs before any launch; on failure nothing is enqueued.
 #include "../../include/ssm.h"
+#include <nvtx3/nvToolsExt.h>
 
 #include <cuda_runtime.h>
 
@@ -10,6 +11,15 @@
 #include "internal.h"
 
 namespace {
+// An NVTX range around each compute entry point, so that profilers can attribute
+// kernels to the library call that launched them (a no-op without a profiler).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 
 using ssm::kStatusBytes;
 
@@ -321,6 +331,7 @@ ssm_status ssm_scan_plan(const ssm_scan_args *a, int64_t *chunk_len, int32_t *nc
 }
 
 ssm_status ssm_scan_fwd(const ssm_scan_args *a, ssm_stream_t stream) {
+    NvtxRange nvtx("ssm_scan_fwd");
     ssm_status s = check_scan(a);
     if (s != SSM_OK) return s;
     int64_t cl;
@@ -377,6 +388,7 @@ ssm_status ssm_ssd_plan(const ssm_ssd_args *a, int32_t *tensor_core) {
 }
 
 ssm_status ssm_ssd_chunk_fwd(const ssm_ssd_args *a, ssm_stream_t stream) {
+    NvtxRange nvtx("ssm_ssd_chunk_fwd");
     ssm_status s = check_ssd(a);
     if (s != SSM_OK) return s;
     ssm::SSDParams p = ssd_params(a);
@@ -390,6 +402,7 @@ ssm_status ssm_ssd_chunk_fwd(const ssm_ssd_args *a, ssm_stream_t stream) {
 }
 
 ssm_status ssm_step_decode(const ssm_decode_args *a, ssm_stream_t stream) {
+    NvtxRange nvtx("ssm_step_decode");
     ssm_status s = check_decode(a);
     if (s != SSM_OK) return s;
     if (a->batch * a->dim == 0) return SSM_OK;
@@ -414,6 +427,7 @@ ssm_status ssm_step_decode(const ssm_decode_args *a, ssm_stream_t stream) {
 }
 
 ssm_status ssm_ssd_step_decode(const ssm_ssd_decode_args *a, ssm_stream_t stream) {
+    NvtxRange nvtx("ssm_ssd_step_decode");
     ssm_status s = check_ssd_decode(a);
     if (s != SSM_OK) return s;
     if (a->batch == 0) return SSM_OK;
@@ -447,6 +461,7 @@ ssm_status ssm_scan_bwd_workspace_size(const ssm_scan_bwd_args *a, size_t *bytes
 }
 
 ssm_status ssm_scan_bwd(const ssm_scan_bwd_args *a, ssm_stream_t stream) {
+    NvtxRange nvtx("ssm_scan_bwd");
     ssm_status s = check_scan_bwd(a);
     if (s != SSM_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -515,6 +530,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_args *a, ssm_stream_t stream) {
 }
 
 ssm_status ssm_conv1d(const ssm_conv1d_args *a, ssm_stream_t stream) {
+    NvtxRange nvtx("ssm_conv1d");
     ssm_status s = check_conv1d(a);
     if (s != SSM_OK) return s;
     if (a->batch * a->seqlen * a->dim == 0) return SSM_OK;
