@@ -588,6 +588,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches * args.steps,
         "wall_ms_per_step_incl_flush": wall / args.steps * 1e3,
         "ceilings": scan_ceilings(p, algo, hbm, device),
+        "device": torch.cuda.get_device_name(device),
     }
     # end to end on every rank at once (each with its own pinned host buffers): the
     # job's updates over the slowest rank's time
