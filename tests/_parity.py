@@ -48,7 +48,21 @@ def run_ssd(p, chunk=None):
     return host(y), host(hf)
 
 
+def bf16_rounding_floor(ref) -> float:
+    """rel-L2 between the oracle's values and the same values rounded to bf16 (RNE):
+    the error any correctly rounded bf16 output has."""
+    r = torch.from_numpy(np.asarray(ref, np.float64)).to(torch.float32).to(torch.bfloat16)
+    return oracle.rel_l2(r.double().numpy(), ref)
+
+
 def assert_close(got, ref, io, what):
+    """rel-L2 of got against the unrounded fp64 oracle within the tolerance of the I/O
+    type.  For bf16 the bound is never below what rounding the oracle itself to bf16
+    costs (plus 5e-4): on tiny tensors dominated by one value that floor alone can
+    exceed 3e-3, and no correct bf16 result could meet the plain bound there."""
     err = oracle.rel_l2(got, ref)
-    assert err <= TOL[io], f"{what}: rel-L2 {err:.3e} > {TOL[io]:.0e}"
+    tol = TOL[io]
+    if io == "bf16":
+        tol = max(tol, bf16_rounding_floor(ref) + 5e-4)
+    assert err <= tol, f"{what}: rel-L2 {err:.3e} > {tol:.1e}"
     return err
