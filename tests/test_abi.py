@@ -267,3 +267,23 @@ def test_ops_fail_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(bd, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         bd.load_library()
+
+
+def test_header_is_plain_c_and_callable_from_c(lib, tmp_path):
+    """A C99 program compiles against include/ssm.h with -Werror -pedantic, links
+    against the library and runs its host-only entry points."""
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = tmp_path / "probe"
+    libdir = os.path.dirname(ssm.library_path())
+    src = os.path.join(ROOT, "tests", "c_abi_probe.c")
+    build = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                            "-I", os.path.join(ROOT, "include"), src, "-o", str(exe),
+                            "-L", libdir, "-l:" + os.path.basename(ssm.library_path()),
+                            "-Wl,-rpath," + libdir], capture_output=True, text=True)
+    assert build.returncode == 0, build.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0, run.stdout + run.stderr
+    assert "0 failure(s)" in run.stdout
