@@ -543,6 +543,29 @@ def cpu_baseline_scan(p, target_s=10.0, max_s=30.0):
                       f"{p.dstate} ({updates:.3e} updates, {dt:.1f} s, fp64 C + OpenMP)"}
 
 
+def _oracle_timed(fn, units, unit, sample):
+    """The fp64 oracle as it stands on a bounded sample, all host cores."""
+    import oracle
+    t0 = time.perf_counter()
+    fn(oracle.default_threads())
+    dt = time.perf_counter() - t0
+    return {"value": units / dt, "unit": unit, "cores": oracle.default_threads(),
+            "kind": "oracle", "sample": f"{sample} ({dt:.2f} s, fp64 C + OpenMP)"}
+
+
+def _oracle_decode(p, steps=10):
+    import oracle
+    state = p.state0.astype(np.float64)
+    toks = [p.tokens(s) for s in range(steps)]
+
+    def run(th):
+        for tok in toks:
+            oracle.decode_step(state, tok["x"], tok["delta"], p.A, tok["B"], tok["C"], Dv=p.D,
+                               z=tok["z"], bias=p.bias, threads=th)
+    return _oracle_timed(run, steps * p.updates_per_step, "state-updates/s",
+                         f"{steps} steps of the whole batch")
+
+
 def run_ours(args, world, rank, local):
     import torch
     device = torch.device("cuda", local)
@@ -623,8 +646,17 @@ def extras(device, flush, hbm, tf_sus, only=None, iters=None):
         per, launches, _, _ = time_scan(p, n(5), 3, flush, device)
         s = float(np.median(per))
         b = scan_bytes(p.batch, p.seqlen, p.dim, p.dstate, 2)
+        import oracle
+        nch = 64
+        args = p.oracle_args()
+        for k in ("x", "delta", "z"):
+            args[k] = np.ascontiguousarray(getattr(p, k)[:, :, :nch])
+        args["A"], args["Dv"], args["bias"] = p.A[:nch], p.D[:nch], p.bias[:nch]
+        orc = _oracle_timed(lambda th: oracle.scan(**args, threads=th),
+                            p.batch * p.seqlen * nch * p.dstate, "state-updates/s",
+                            f"{nch} of {p.dim} channels, whole sequence")
         return {"ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
-                "hbm_frac": b / s / 1e9 / hbm, "launches": launches}
+                "hbm_frac": b / s / 1e9 / hbm, "launches": launches, "oracle": orc}
 
     def ssd():
         p = W.config_problem(3)
@@ -632,9 +664,20 @@ def extras(device, flush, hbm, tf_sus, only=None, iters=None):
         b = ssd_bytes(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, 2)
         # the tensor-core kernel works in 128-step chunks whatever chunk_size asks for
         fl = ssd_flops(p.batch, p.seqlen, p.heads, p.headdim, p.ngroups, p.dstate, 128)
+        import oracle
+        nh = 4
+        args = p.oracle_args()
+        args["x"] = np.ascontiguousarray(p.x[:1, :, :nh])
+        args["delta"] = np.ascontiguousarray(p.delta[:1, :, :nh])
+        args["Bm"], args["Cm"] = p.B[:1], p.C[:1]
+        args["A"], args["Dv"], args["bias"] = p.A[:nh], p.D[:nh], p.bias[:nh]
+        orc = _oracle_timed(lambda th: oracle.ssd(**args, threads=th),
+                            p.seqlen * nh * p.headdim * p.dstate, "state-updates/s",
+                            f"batch row 0, {nh} of {p.heads} heads, whole sequence")
         return {"ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
                 "hbm_frac": b / s / 1e9 / hbm, "tensor_tflops": fl / s / 1e12,
-                "tensor_frac_sustained": fl / s / 1e12 / tf_sus, "kernel_chunk": 128}
+                "tensor_frac_sustained": fl / s / 1e12 / tf_sus, "kernel_chunk": 128,
+                "oracle": orc}
 
     def decode():
         p = W.config_problem(4)
@@ -645,26 +688,50 @@ def extras(device, flush, hbm, tf_sus, only=None, iters=None):
                 "updates_per_s": p.updates_per_step / s_flush,
                 "gbs_l2_flushed": b / s_flush / 1e9, "hbm_frac_l2_flushed": b / s_flush / 1e9 / hbm,
                 "gbs_back_to_back": b / s_hot / 1e9,
-                "note": "back-to-back steps keep much of the 84 MB state in the 126 MB L2"}
+                "note": "back-to-back steps keep much of the 84 MB state in the 126 MB L2",
+                "oracle": _oracle_decode(p)}
 
     def ssd_decode():
         s = time_ssd_decode(64, 80, 64, 1, 128, flush, device, iters=n(30))
         b = ssd_decode_bytes_per_step(64, 80, 64, 1, 128, 2)
+        import oracle
+        q = W.ssd_problem(64, 1, 80, 64, 1, 128, io="bf16", seed=1005, h0=True)
+        state = q.h0.astype(np.float64)
+        orc = _oracle_timed(
+            lambda th: [oracle.ssd_decode_step(state, q.x[:, 0], q.delta[:, 0], q.A, q.B[:, 0],
+                                               q.C[:, 0], Dv=q.D, bias=q.bias, threads=th)
+                        for _ in range(3)],
+            3 * 64 * 80 * 64 * 128, "state-updates/s", "3 steps of the whole batch")
         return {"ms_per_step_l2_flushed": s * 1e3, "updates_per_s": 64 * 80 * 64 * 128 / s,
-                "gbs_l2_flushed": b / s / 1e9, "hbm_frac_l2_flushed": b / s / 1e9 / hbm}
+                "gbs_l2_flushed": b / s / 1e9, "hbm_frac_l2_flushed": b / s / 1e9 / hbm,
+                "oracle": orc}
 
     def conv1d():
         s = time_conv1d(8, 2048, 1536, 4, flush, device, iters=n(30))
         b = conv1d_bytes(8, 2048, 1536, 4, 2)
-        return {"ms": s * 1e3, "gbs": b / s / 1e9, "hbm_frac": b / s / 1e9 / hbm}
+        import oracle
+        rng = np.random.default_rng(1006)
+        x = rng.standard_normal((8, 2048, 1536))
+        w = rng.standard_normal((1536, 4)) / 2
+        orc = _oracle_timed(lambda th: oracle.conv1d(x, w, threads=th), 8 * 2048 * 1536,
+                            "outputs/s", "the whole block shape")
+        return {"ms": s * 1e3, "gbs": b / s / 1e9, "hbm_frac": b / s / 1e9 / hbm,
+                "outputs_per_s": 8 * 2048 * 1536 / s, "oracle": orc}
 
     def scan_bwd():
         p = W.config_problem(1)
         s = time_scan_bwd(p, flush, device, iters=n(10))
         b = scan_bwd_bytes(p.batch, p.seqlen, p.dim, p.dstate, 2)
+        import oracle
+        gy = np.random.default_rng(7).standard_normal((1, p.seqlen, p.dim))
+        orc = _oracle_timed(
+            lambda th: oracle.scan_bwd(gy, p.x[:1], p.delta[:1], p.A, p.B[:1], p.C[:1],
+                                       Dv=p.D, z=p.z[:1], bias=p.bias, threads=th),
+            p.seqlen * p.dim * p.dstate, "state-updates/s", "batch row 0 of 8")
         return {"ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
                 "hbm_frac": b / s / 1e9 / hbm,
-                "note": "states recomputed: a checkpoint pass and a reverse pass"}
+                "note": "states recomputed: a checkpoint pass and a reverse pass",
+                "oracle": orc}
 
     runners = {
         "scan_bf16_B1_D2048_L131072_N16": scan_long,
