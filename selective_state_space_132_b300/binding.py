@@ -522,3 +522,44 @@ def conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] =
                       0 if workspace is None else workspace.numel() * workspace.element_size())
     _raise(lib.ssm_conv1d(ctypes.byref(args), _stream(stream)), "ssm_conv1d")
     return out
+
+
+# ---------------------------------------------------------------- autograd
+class SelectiveScanFn(torch.autograd.Function):
+    """scan_fwd with its gradients from scan_bwd (hidden states recomputed in the
+    backward pass, nothing but the inputs kept from the forward)."""
+
+    @staticmethod
+    def forward(ctx, x, delta, A, B, C, D, z, delta_bias, h0, delta_softplus, discretization):
+        y, h_final = scan_fwd(x, delta, A, B, C, D=D, z=z, delta_bias=delta_bias,
+                              delta_softplus=delta_softplus, h0=h0,
+                              discretization=discretization)
+        ctx.save_for_backward(x, delta, A, B, C, D, z, delta_bias, h0)
+        ctx.delta_softplus, ctx.discretization = delta_softplus, discretization
+        return y, h_final
+
+    @staticmethod
+    def backward(ctx, dy, dh_final):
+        x, delta, A, B, C, D, z, delta_bias, h0 = ctx.saved_tensors
+        g = scan_bwd(dy.contiguous().to(x.dtype), x, delta, A, B, C, D=D, z=z,
+                     delta_bias=delta_bias, delta_softplus=ctx.delta_softplus, h0=h0,
+                     dh_final=None if dh_final is None else dh_final.contiguous().float(),
+                     discretization=ctx.discretization)
+
+        def cast(grad, like):
+            return None if like is None else grad.to(like.dtype)
+        return (g["dx"], g["ddelta"], g["dA"], cast(g["dB"], B), cast(g["dC"], C),
+                cast(g["dD"], D), g.get("dz"), cast(g["ddelta_bias"], delta_bias),
+                cast(g["dh0"], h0), None, None)
+
+
+def selective_scan(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                   C: torch.Tensor, D: Optional[torch.Tensor] = None,
+                   z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
+                   h0: Optional[torch.Tensor] = None, delta_softplus: bool = True,
+                   discretization: str = "euler") -> Tuple[torch.Tensor, torch.Tensor]:
+    """Differentiable selective scan: (y, h_final) = scan_fwd(...), with every input's
+    gradient from the library's backward kernel.  Shapes and dtypes as scan_fwd; the
+    gradients of B and C (fp32 sums over channels) are returned in B's and C's dtype."""
+    return SelectiveScanFn.apply(x, delta, A, B, C, D, z, delta_bias, h0, delta_softplus,
+                                 discretization)
