@@ -177,7 +177,12 @@ SSM_API ssm_status ssm_scan_bwd(const ssm_scan_bwd_args *args, ssm_stream_t stre
  *   - Every call on a device shares the one buffer and leaves its contents behind;
  *     the call clears what must start at zero itself.  Calls whose work overlaps
  *     on the GPU (other streams, other host threads) race on the buffer: order
- *     them on one stream or synchronise between them. */
+ *     them on one stream or synchronise between them.
+ *   - The device status word that ssm_scan_fwd keeps at the start of the caller's
+ *     workspace sits at the start of the library's buffer here, where the caller
+ *     cannot read it (ssm_read_device_status needs a caller pointer) and the next
+ *     call clears it: a bounded wait that runs out inside this call's kernels is not
+ *     reported.  Callers that need that report use ssm_scan_fwd with a workspace. */
 #define SSM_NOALLOC_SCRATCH_BYTES (4u << 20)
 SSM_API ssm_status ssm_scan_fwd_noalloc(const ssm_scan_args *args, ssm_stream_t stream);
 

@@ -182,10 +182,17 @@ def _check(t: Optional[torch.Tensor], name: str, shape, dtype, device):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _stream(stream) -> Optional[int]:
+def _stream(stream, device=None) -> Optional[int]:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _launch(fn, args, stream, device, where: str):
+    """Call a compute entry point with the tensors' device current (the library
+    launches on the current device) and, by default, that device's current stream."""
+    with torch.cuda.device(device):
+        _raise(fn(ctypes.byref(args), _stream(stream, device)), where)
 
 
 def _raise(rc: int, where: str):
@@ -281,7 +288,7 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
            "ssm_scan_workspace_size")
     ws, nbytes = _workspace(int(need.value), x.device, workspace)
     args.workspace, args.workspace_bytes = _ptr(ws), nbytes
-    _raise(lib.ssm_scan_fwd(ctypes.byref(args), _stream(stream)), "ssm_scan_fwd")
+    _launch(lib.ssm_scan_fwd, args, stream, x.device, "ssm_scan_fwd")
     return y, h_final
 
 
@@ -321,7 +328,7 @@ def scan_bwd(dy: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torch.Te
            "ssm_scan_bwd_workspace_size")
     ws, nbytes = _workspace(int(need.value), dev, workspace)
     args.workspace, args.workspace_bytes = _ptr(ws), nbytes
-    _raise(lib.ssm_scan_bwd(ctypes.byref(args), _stream(stream)), "ssm_scan_bwd")
+    _launch(lib.ssm_scan_bwd, args, stream, x.device, "ssm_scan_bwd")
     if z is None:
         del g["dz"]
     return g
@@ -341,16 +348,15 @@ NOALLOC_SCRATCH_BYTES = 4 << 20
 
 def scan_fwd_noalloc(x, delta, A, B, C, D=None, z=None, delta_bias=None,
                      delta_softplus: bool = True, h0=None, y=None, h_final=None,
-                     time_chunk: int = 0, stream=None):
+                     time_chunk: int = 0, stream=None, discretization: str = "euler"):
     """ssm_scan_fwd_noalloc: the scan with the library's fixed scratch buffer instead
     of a workspace, for callers that must not allocate device memory per call.
     Outputs y and h_final must be passed in (nothing is allocated here either)."""
     if y is None:
         raise ValueError("scan_fwd_noalloc allocates nothing: pass y (and h_final if wanted)")
     args = _scan_args(x, delta, A, B, C, D, z, delta_bias, delta_softplus, h0, y, h_final,
-                      time_chunk)
-    _raise(load_library().ssm_scan_fwd_noalloc(ctypes.byref(args), _stream(stream)),
-           "ssm_scan_fwd_noalloc")
+                      time_chunk, discretization)
+    _launch(load_library().ssm_scan_fwd_noalloc, args, stream, x.device, "ssm_scan_fwd_noalloc")
     return y, h_final
 
 
@@ -420,14 +426,17 @@ def ssd_chunk_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torc
            "ssm_ssd_workspace_size")
     ws, nbytes = _workspace(int(need.value), x.device, workspace)
     args.workspace, args.workspace_bytes = _ptr(ws), nbytes
-    _raise(lib.ssm_ssd_chunk_fwd(ctypes.byref(args), _stream(stream)), "ssm_ssd_chunk_fwd")
+    _launch(lib.ssm_ssd_chunk_fwd, args, stream, x.device, "ssm_ssd_chunk_fwd")
     return y, h_final
 
 
 def read_device_status(workspace: torch.Tensor, stream=None) -> int:
     out = ctypes.c_int(0)
-    _raise(load_library().ssm_read_device_status(_ptr(workspace), _stream(stream),
-                                                 ctypes.byref(out)), "ssm_read_device_status")
+    with torch.cuda.device(workspace.device):
+        _raise(load_library().ssm_read_device_status(_ptr(workspace),
+                                                     _stream(stream, workspace.device),
+                                                     ctypes.byref(out)),
+               "ssm_read_device_status")
     return int(out.value)
 
 
@@ -459,7 +468,7 @@ def step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: to
                       _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
                       _ptr(delta_bias), _ptr(y))
     args.discretization = _disc(discretization)
-    _raise(lib.ssm_step_decode(ctypes.byref(args), _stream(stream)), "ssm_step_decode")
+    _launch(lib.ssm_step_decode, args, stream, x.device, "ssm_step_decode")
     return y
 
 
@@ -492,7 +501,7 @@ def ssd_step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A
     args = SSDDecodeArgs(nb, H, P, G, N, _io_code(x), int(bool(delta_softplus)), _ptr(state),
                          _ptr(x), _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
                          _ptr(delta_bias), _ptr(y))
-    _raise(lib.ssm_ssd_step_decode(ctypes.byref(args), _stream(stream)), "ssm_ssd_step_decode")
+    _launch(lib.ssm_ssd_step_decode, args, stream, x.device, "ssm_ssd_step_decode")
     return y
 
 
@@ -520,7 +529,7 @@ def conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] =
     args = Conv1dArgs(nb, L, Dm, K, _io_code(x), int(bool(silu)), _ptr(x), _ptr(x_prev),
                       _ptr(weight), _ptr(bias), _ptr(out), _ptr(workspace),
                       0 if workspace is None else workspace.numel() * workspace.element_size())
-    _raise(lib.ssm_conv1d(ctypes.byref(args), _stream(stream)), "ssm_conv1d")
+    _launch(lib.ssm_conv1d, args, stream, x.device, "ssm_conv1d")
     return out
 
 
@@ -541,16 +550,21 @@ class SelectiveScanFn(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dy, dh_final):
         x, delta, A, B, C, D, z, delta_bias, h0 = ctx.saved_tensors
+        need = ctx.needs_input_grad
+        if not any(need[:9]):
+            return (None,) * 11
         g = scan_bwd(dy.contiguous().to(x.dtype), x, delta, A, B, C, D=D, z=z,
                      delta_bias=delta_bias, delta_softplus=ctx.delta_softplus, h0=h0,
                      dh_final=None if dh_final is None else dh_final.contiguous().float(),
                      discretization=ctx.discretization)
 
-        def cast(grad, like):
-            return None if like is None else grad.to(like.dtype)
-        return (g["dx"], g["ddelta"], g["dA"], cast(g["dB"], B), cast(g["dC"], C),
-                cast(g["dD"], D), g.get("dz"), cast(g["ddelta_bias"], delta_bias),
-                cast(g["dh0"], h0), None, None)
+        def out(i, grad, like):
+            # only the inputs autograd asked for get a gradient
+            return grad.to(like.dtype) if (need[i] and like is not None) else None
+        return (out(0, g["dx"], x), out(1, g["ddelta"], delta), out(2, g["dA"], A),
+                out(3, g["dB"], B), out(4, g["dC"], C), out(5, g["dD"], D),
+                out(6, g.get("dz"), z), out(7, g["ddelta_bias"], delta_bias),
+                out(8, g["dh0"], h0), None, None)
 
 
 def selective_scan(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,

@@ -9,6 +9,7 @@ include/ssm.h.
 from __future__ import annotations
 
 import argparse
+import concurrent.futures
 import os
 import subprocess
 import sys
@@ -53,16 +54,22 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if verbose:
         flags += ["-Xptxas", "-v"]
     flags += list(extra_flags or [])
-    objs = []
-    for src in sources():
+    def compile_one(src):
         obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc()] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
-        if verbose or r.returncode != 0:
-            sys.stderr.write(r.stdout + r.stderr)
-        if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {os.path.basename(src)}")
-        objs.append(obj)
+        return src, obj, r
+
+    # the translation units are independent: compile them side by side
+    objs = []
+    workers = max(1, min(len(sources()), os.cpu_count() or 1))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as pool:
+        for src, obj, r in pool.map(compile_one, sources()):
+            if verbose or r.returncode != 0:
+                sys.stderr.write(r.stdout + r.stderr)
+            if r.returncode != 0:
+                raise RuntimeError(f"nvcc failed on {os.path.basename(src)}")
+            objs.append(obj)
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -10,7 +10,7 @@ import oracle
 import selective_state_space_132_b300 as ssm
 from selective_state_space_132_b300 import workloads as W
 
-from _parity import assert_close, dev, host, io_dtype, run_scan, run_ssd
+from _parity import assert_close, dev, host, io_dtype, run_scan, run_ssd, ssd_tc_allowance
 
 pytestmark = pytest.mark.gpu
 
@@ -49,10 +49,11 @@ def test_scan(io, kind, N):
 def test_ssd_tensor_core(kind):
     p = _degenerate(W.ssd_problem(1, 300, 4, 64, 1, 128, chunk=128, io="bf16", seed=51, h0=True),
                     kind)
+    ay, ah = ssd_tc_allowance(p)
     y, hf = run_ssd(p)
     yr, hr = oracle.ssd(**p.oracle_args())
-    assert_close(y, yr, "bf16", f"y ({kind})")
-    assert_close(hf, hr, "bf16", f"h_final ({kind})")
+    assert_close(y, yr, "bf16", f"y ({kind})", allow=ay)
+    assert_close(hf, hr, "bf16", f"h_final ({kind})", allow=ah)
 
 
 @pytest.mark.parametrize("kind", ["zero_step", "huge_step", "no_decay"])

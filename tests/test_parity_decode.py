@@ -7,7 +7,7 @@ import oracle
 import selective_state_space_132_b300 as ssm
 from selective_state_space_132_b300 import workloads as W
 
-from _parity import assert_close, dev, host, io_dtype
+from _parity import Parity, assert_close, dev, host, io_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -61,12 +61,26 @@ def test_decode_equals_scan():
 
 
 @pytest.mark.slow
-def test_decode_full_size_sampled_rows():
+def test_decode_full_size():
     """Reference workload: batch 256, d_inner 5120, N 16, fp32 state, bf16 tokens, 1000
-    steps in place; every step's y and the final state are checked on 6 sampled
-    sequences against the streaming oracle."""
+    steps in place; every step's y for every sequence and channel, and the whole final
+    state, against the streaming oracle.  Rows are the (b, d) channels over the steps."""
     p = W.config_problem(4)
-    _decode_run(p, p.steps, rows=[0, 1, 77, 128, 200, 255])
+    io = io_dtype(p.io)
+    state = dev(p.state0)
+    A, Dv, bias = dev(p.A), dev(p.D), dev(p.bias)
+    ref_state = p.state0.astype(np.float64).copy()
+    rows = p.batch * p.dim
+    py = Parity(p.io, "y (decode, 1000 steps)", rows)
+    for s in range(p.steps):
+        tok = p.tokens(s)
+        y = ssm.step_decode(state, dev(tok["x"], io), dev(tok["delta"], io), A, dev(tok["B"], io),
+                            dev(tok["C"], io), D=Dv, z=dev(tok["z"], io), delta_bias=bias)
+        yr = oracle.decode_step(ref_state, tok["x"], tok["delta"], p.A, tok["B"], tok["C"],
+                                Dv=p.D, z=tok["z"], bias=p.bias, softplus=True)
+        py.add(host(y).reshape(rows, 1), yr.reshape(rows, 1))
+    py.check()
+    assert_close(host(state), ref_state, p.io, "state after 1000 steps")
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
