@@ -4,11 +4,13 @@
                     [--workload NAME] [--no-extras] [--no-cpu]
 
 One step = one forward pass of the S6 scan (softplus step, exp decay, state
-recurrence, C readout, D skip, SiLU gate) over one batch of the 130M-layer
-workload (batch 8, d_inner 1536, L 2048, N 16, bf16 I/O, fp32 state), inputs
-already resident in HBM, L2 flushed before every step (a 256 MB write, then a 256 MB
-read so that the lines left in L2 are clean).  The
-metric is state updates per second (B*L*D*N / time).  Rank 0 prints one JSON
+recurrence, C readout, D skip, SiLU gate, and the carry between time chunks) over
+one batch of the long-context workload (batch 1, d_inner 2048, L 131072, N 16, bf16
+I/O, fp32 state: the largest scan configuration, 2.15 GB of inputs and outputs),
+inputs already resident in HBM, L2 flushed before every step (a 256 MB write, then a
+256 MB read so that the lines left in L2 are clean).  `--workload` selects the
+130M-layer shape instead (batch 8, d_inner 1536, L 2048, N 16).  The metric is
+state updates per second (B*L*D*N / time).  Rank 0 prints one JSON
 line.  Under torchrun (N > 1) every rank runs its own independent batch (the
 chains of the scan are independent: no data-path collective), so scaling is
 weak and `value` is the updates of all ranks over the slowest rank's time.
@@ -94,10 +96,16 @@ def scan_ceilings(p, algo_bytes, hbm_gbs, device):
     rows = p.batch * p.seqlen * p.dim
     mufu = (units + 3 * rows) / (sms * MUFU_EX2_PER_CLK * clk)
     fp32 = 4 * units / (sms * FFMA_PER_CLK * clk)
+    # instruction dispatch: per update at least 4 fp32 operations (one cycle per warp
+    # instruction each) and one ex2 (two cycles), 32 lanes per SM sub-partition
+    dispatch = 6 * units / 32 / (sms * 4 * clk)
     hbm = algo_bytes / (hbm_gbs * 1e9)
-    return {"mufu_us": mufu * 1e6, "fp32_us": fp32 * 1e6, "hbm_us": hbm * 1e6, "sms": sms,
+    return {"mufu_us": mufu * 1e6, "fp32_us": fp32 * 1e6, "dispatch_us": dispatch * 1e6,
+            "hbm_us": hbm * 1e6, "sms": sms,
             "basis": "per-SM rates measured on B300: ex2 29.7 lanes/clk, FFMA 113/clk; "
-                     "2032 MHz"}
+                     "ex2 and fp32x2 take two dispatch cycles per warp instruction, FFMA one "
+                     "(recurrence-core probe: 103.5 cycles per 16-state warp step at four "
+                     "warps per sub-partition); 2032 MHz"}
 
 
 def scan_bytes(nb, L, D, N, e, gate=True, h0=False):
@@ -226,6 +234,16 @@ def aggregate(units_per_rank: float, seconds_max: float, world: int) -> float:
 
 
 # ------------------------------------------------------------------ our arm
+def bench_config(workload, p, world):
+    """The `config` object of the JSON line, the same in both arms."""
+    return {"workload": workload, "batch": p.batch, "seqlen": p.seqlen, "d_inner": p.dim,
+            "d_state": p.dstate, "io": p.io, "state": "fp32", "gate": True,
+            "l2": "flushed before every step (256 MB write, then 256 MB read); the inputs "
+                  f"({scan_bytes(p.batch, p.seqlen, p.dim, p.dstate, 2 if p.io == 'bf16' else 4) / 1e9:.2f} GB) "
+                  "also exceed the 126 MB L2",
+            "parallelism": f"replicas x{world} (independent batches per GPU)"}
+
+
 def _to_dev(device):
     import torch
 
@@ -277,10 +295,13 @@ def e2e_scan(p, steps, device, slices=8):
     """Same metric through the public API with pinned host buffers: every step copies
     the inputs host->device, runs the scan and reads y and the final state back.
 
-    The batch is cut into `slices` row slices that flow through three streams: while
-    slice i is scanned, slice i + 1 is copied in and slice i - 1 is copied out (PCIe
-    carries both directions at once).  Events order the reuse of each slice's device
-    buffers across steps.  Timed by the host clock, synchronised on both sides."""
+    The work is cut into `slices` pieces that flow through three streams: while piece
+    i is scanned, piece i + 1 is copied in and piece i - 1 is copied out (PCIe carries
+    both directions at once).  Pieces are batch rows when the batch has enough of them,
+    else stretches of time (batch 1: contiguous), the state handed from one stretch to
+    the next through h0 / h_final of the public call.  Events order the reuse of each
+    piece's device buffers across steps.  Timed by the host clock, synchronised on
+    both sides."""
     import torch
     import selective_state_space_132_b300 as ssm
 
@@ -299,9 +320,15 @@ def e2e_scan(p, steps, device, slices=8):
     dx, ddl, dz, dB, dC = (torch.empty(a.shape, dtype=a.dtype, device=device)
                            for a in (hx, hdl, hz, hB, hC))
     dy = torch.empty(hx.shape, dtype=io, device=device)
-    dh = torch.empty(hh.shape, dtype=torch.float32, device=device)
-    n = max(1, min(slices, p.batch))
-    bounds = [(p.batch * i // n, p.batch * (i + 1) // n) for i in range(n)]
+    by_time = p.batch < slices and p.batch == 1
+    n = max(1, min(slices, p.seqlen if by_time else p.batch))
+    extent = p.seqlen if by_time else p.batch
+    bounds = [(extent * i // n, extent * (i + 1) // n) for i in range(n)]
+    # final state of each piece (time pieces chain through them); the last is the result
+    dh = [torch.empty(hh.shape, dtype=torch.float32, device=device) for _ in bounds]
+
+    def sl(a, b0, b1):
+        return a[:, b0:b1] if by_time else a[b0:b1]
     s_in, s_run, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev_in = [torch.cuda.Event() for _ in bounds]
     ev_run = [torch.cuda.Event() for _ in bounds]
@@ -314,21 +341,30 @@ def e2e_scan(p, steps, device, slices=8):
     def step():
         for i, (b0, b1) in enumerate(bounds):
             with torch.cuda.stream(s_in):
-                s_in.wait_event(ev_run[i])         # the previous scan of this slice is done
+                s_in.wait_event(ev_run[i])         # the previous scan of this piece is done
                 for d_, h_ in ((dx, hx), (ddl, hdl), (dz, hz), (dB, hB), (dC, hC)):
-                    d_[b0:b1].copy_(h_[b0:b1], non_blocking=True)
+                    sl(d_, b0, b1).copy_(sl(h_, b0, b1), non_blocking=True)
                 ev_in[i].record(s_in)
             with torch.cuda.stream(s_run):
                 s_run.wait_event(ev_in[i])
-                s_run.wait_event(ev_out[i])        # the previous outputs left this slice
-                ssm.scan_fwd(dx[b0:b1], ddl[b0:b1], A, dB[b0:b1], dC[b0:b1], D=Dv,
-                             z=dz[b0:b1], delta_bias=bias, y=dy[b0:b1], h_final=dh[b0:b1],
-                             stream=s_run)
+                s_run.wait_event(ev_out[i])        # the previous outputs left this piece
+                if by_time:
+                    ssm.scan_fwd(sl(dx, b0, b1), sl(ddl, b0, b1), A, sl(dB, b0, b1),
+                                 sl(dC, b0, b1), D=Dv, z=sl(dz, b0, b1), delta_bias=bias,
+                                 h0=dh[i - 1] if i > 0 else None, y=sl(dy, b0, b1),
+                                 h_final=dh[i], stream=s_run)
+                else:
+                    ssm.scan_fwd(dx[b0:b1], ddl[b0:b1], A, dB[b0:b1], dC[b0:b1], D=Dv,
+                                 z=dz[b0:b1], delta_bias=bias, y=dy[b0:b1],
+                                 h_final=dh[0][b0:b1], stream=s_run)
                 ev_run[i].record(s_run)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_run[i])
-                hy[b0:b1].copy_(dy[b0:b1], non_blocking=True)
-                hh[b0:b1].copy_(dh[b0:b1], non_blocking=True)
+                sl(hy, b0, b1).copy_(sl(dy, b0, b1), non_blocking=True)
+                if by_time and i == n - 1:
+                    hh.copy_(dh[i], non_blocking=True)
+                elif not by_time:
+                    hh[b0:b1].copy_(dh[0][b0:b1], non_blocking=True)
                 ev_out[i].record(s_out)
 
     for _ in range(2):
@@ -338,7 +374,8 @@ def e2e_scan(p, steps, device, slices=8):
     for _ in range(steps):
         step()
     torch.cuda.synchronize(device)
-    return (time.perf_counter() - t0) / steps, h2d, d2h, n
+    kind = "time stretches (state chained through h0 / h_final)" if by_time else "batch slices"
+    return (time.perf_counter() - t0) / steps, h2d, d2h, f"{n} {kind}"
 
 
 class L2Flush:
@@ -395,25 +432,29 @@ def time_ssd(p, iters, flush, device):
     return _median_event_time(step, flush, iters)
 
 
-def time_decode(p, steps, flush, device, pool=8):
-    """Per-step time of ssm_step_decode with the state in place; tokens cycle through a
-    pool of `pool` pre-generated steps.  Returns (median with L2 flushed before each
-    step, mean over back-to-back steps)."""
+def time_decode(p, steps, flush, device):
+    """Per-step time of ssm_step_decode with the state in place over `steps` distinct
+    token steps, all generated on the device before timing (the recipe's distributions,
+    torch's seeded generator; about 7.9 MB per step).  Returns (median with L2 flushed
+    before each of the first 50 steps, mean over all steps back to back)."""
     import torch
     import selective_state_space_132_b300 as ssm
     io = torch.bfloat16
     t = _to_dev(device)
     state = t(p.state0)
     A, Dv, bias = t(p.A), t(p.D), t(p.bias)
-    toks = []
-    for s in range(pool):
-        k = p.tokens(s)
-        toks.append({n: t(v, io) for n, v in k.items()})
+    g = torch.Generator(device=device)
+    g.manual_seed(p.seed)
+    shp = (steps, p.batch, p.dim)
+    xs = torch.randn(shp, generator=g, device=device).to(io)
+    dls = (0.5 * torch.randn(shp, generator=g, device=device)).to(io)
+    zs = torch.randn(shp, generator=g, device=device).to(io)
+    Bs = torch.randn((steps, p.batch, p.dstate), generator=g, device=device).to(io)
+    Cs = torch.randn((steps, p.batch, p.dstate), generator=g, device=device).to(io)
     y = torch.empty((p.batch, p.dim), dtype=io, device=device)
 
     def step(i):
-        k = toks[i % pool]
-        ssm.step_decode(state, k["x"], k["delta"], A, k["B"], k["C"], D=Dv, z=k["z"],
+        ssm.step_decode(state, xs[i], dls[i], A, Bs[i], Cs[i], D=Dv, z=zs[i],
                         delta_bias=bias, y=y)
     for i in range(3):
         step(i)
@@ -515,32 +556,41 @@ def time_scan_bwd(p, flush, device, iters=10):
 
 
 def cpu_baseline_scan(p, target_s=10.0, max_s=30.0):
-    """The fp64 oracle as it stands, all host cores, on a bounded channel sample of
-    the workload; returns updates/s and what the sample was."""
+    """The fp64 oracle as it stands on a bounded channel sample of the workload: on all
+    host cores (the reported value) and on one core; returns updates/s and what the
+    samples were."""
     import oracle
     threads = oracle.default_threads()
 
-    def run(nch):
+    def run(nch, th):
         args = p.oracle_args()
         sel = slice(0, nch)
         for k in ("x", "delta", "z"):
             args[k] = np.ascontiguousarray(getattr(p, k)[:, :, sel])
         args["A"], args["Dv"], args["bias"] = p.A[sel], p.D[sel], p.bias[sel]
         t0 = time.perf_counter()
-        oracle.scan(**args, threads=threads)
+        oracle.scan(**args, threads=th)
         return time.perf_counter() - t0
-    nch = min(p.dim, 16)
-    dt = run(nch)
-    while dt < target_s / 4 and nch < p.dim:
-        nch = min(p.dim, nch * 4)
-        dt = run(nch)
-        if dt > max_s:
-            break
+
+    def sample(th, goal):
+        nch = min(p.dim, 16)
+        dt = run(nch, th)
+        while dt < goal / 4 and nch < p.dim:
+            nch = min(p.dim, nch * 4)
+            dt = run(nch, th)
+            if dt > max_s:
+                break
+        return nch, dt
+    nch, dt = sample(threads, target_s)
+    n1, dt1 = sample(1, target_s / 2)
     updates = p.batch * p.seqlen * nch * p.dstate
+    upd1 = p.batch * p.seqlen * n1 * p.dstate
     return {"value": updates / dt, "unit": "state-updates/s", "cores": threads,
             "kind": "oracle",
             "sample": f"batch {p.batch} x L {p.seqlen} x {nch} of {p.dim} channels x N "
-                      f"{p.dstate} ({updates:.3e} updates, {dt:.1f} s, fp64 C + OpenMP)"}
+                      f"{p.dstate} ({updates:.3e} updates, {dt:.1f} s, fp64 C + OpenMP)",
+            "value_1_thread": upd1 / dt1,
+            "sample_1_thread": f"{n1} channels ({upd1:.3e} updates, {dt1:.1f} s, one core)"}
 
 
 def _oracle_timed(fn, units, unit, sample):
@@ -600,10 +650,7 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": sec_per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; reference recipe)",
-        "config": {"workload": args.workload, "batch": p.batch, "seqlen": p.seqlen,
-                   "d_inner": p.dim, "d_state": p.dstate, "io": p.io, "state": "fp32",
-                   "gate": True, "l2": "flushed before every step (256 MB write, then 256 MB read)",
-                   "parallelism": f"replicas x{world} (independent batches per GPU)"},
+        "config": bench_config(args.workload, p, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": PROFILED_TRAFFIC.get(src_hash),
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": algo,
@@ -623,16 +670,16 @@ def run_ours(args, world, rank, local):
         out["e2e"] = {"value": aggregate(units, e2e_max, world), "unit": "state-updates/s",
                       "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
                       "ms_per_step": e2e_max * 1e3,
-                      "pipeline": f"{nslices} batch slices; copy in, scan and copy out on "
-                                  "three streams"}
+                      "pipeline": f"{nslices}; copy in, scan and copy out on three "
+                                  "streams"}
         if world == 1 and not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline_scan(p)
         if not args.no_extras and world == 1:
-            out["kernels"] = extras(device, flush, hbm, tf_sus)
+            out["kernels"] = extras(device, flush, hbm, tf_sus, skip=(args.workload,))
     return out
 
 
-def extras(device, flush, hbm, tf_sus, only=None, iters=None):
+def extras(device, flush, hbm, tf_sus, only=None, iters=None, skip=()):
     """The other workloads, one measurement each (parity cases, not the bench line).
     `only` runs one of them alone and `iters` sets its timed iterations (both used to
     profile one kernel with ncu)."""
@@ -641,22 +688,23 @@ def extras(device, flush, hbm, tf_sus, only=None, iters=None):
     def n(default):
         return default if iters is None else iters
 
-    def scan_long():
-        p = W.config_problem(2)
-        per, launches, _, _ = time_scan(p, n(5), 3, flush, device)
-        s = float(np.median(per))
-        b = scan_bytes(p.batch, p.seqlen, p.dim, p.dstate, 2)
-        import oracle
-        nch = 64
-        args = p.oracle_args()
-        for k in ("x", "delta", "z"):
-            args[k] = np.ascontiguousarray(getattr(p, k)[:, :, :nch])
-        args["A"], args["Dv"], args["bias"] = p.A[:nch], p.D[:nch], p.bias[:nch]
-        orc = _oracle_timed(lambda th: oracle.scan(**args, threads=th),
-                            p.batch * p.seqlen * nch * p.dstate, "state-updates/s",
-                            f"{nch} of {p.dim} channels, whole sequence")
-        return {"ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
-                "hbm_frac": b / s / 1e9 / hbm, "launches": launches, "oracle": orc}
+    def scan_cfg(index, nch):
+        def run():
+            p = W.config_problem(index)
+            per, launches, _, _ = time_scan(p, n(5 if index == 2 else 20), 3, flush, device)
+            s = float(np.median(per))
+            b = scan_bytes(p.batch, p.seqlen, p.dim, p.dstate, 2)
+            import oracle
+            args = p.oracle_args()
+            for k in ("x", "delta", "z"):
+                args[k] = np.ascontiguousarray(getattr(p, k)[:, :, :nch])
+            args["A"], args["Dv"], args["bias"] = p.A[:nch], p.D[:nch], p.bias[:nch]
+            orc = _oracle_timed(lambda th: oracle.scan(**args, threads=th),
+                                p.batch * p.seqlen * nch * p.dstate, "state-updates/s",
+                                f"{nch} of {p.dim} channels, whole sequence")
+            return {"ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
+                    "hbm_frac": b / s / 1e9 / hbm, "launches": launches, "oracle": orc}
+        return run
 
     def ssd():
         p = W.config_problem(3)
@@ -688,7 +736,8 @@ def extras(device, flush, hbm, tf_sus, only=None, iters=None):
                 "updates_per_s": p.updates_per_step / s_flush,
                 "gbs_l2_flushed": b / s_flush / 1e9, "hbm_frac_l2_flushed": b / s_flush / 1e9 / hbm,
                 "gbs_back_to_back": b / s_hot / 1e9,
-                "note": "back-to-back steps keep much of the 84 MB state in the 126 MB L2",
+                "note": "1000 distinct token steps; back-to-back steps keep much of the 84 MB "
+                        "state in the 126 MB L2",
                 "oracle": _oracle_decode(p)}
 
     def ssd_decode():
@@ -734,7 +783,8 @@ def extras(device, flush, hbm, tf_sus, only=None, iters=None):
                 "oracle": orc}
 
     runners = {
-        "scan_bf16_B1_D2048_L131072_N16": scan_long,
+        "scan_bf16_B8_D1536_L2048_N16": scan_cfg(1, 256),
+        "scan_bf16_B1_D2048_L131072_N16": scan_cfg(2, 64),
         "ssd_bf16_B4_L8192_H80_P64_N128_G1_Q256": ssd,
         "decode_bf16_B256_D5120_N16_x1000": decode,
         "ssd_decode_bf16_B64_H80_P64_N128": ssd_decode,
@@ -745,7 +795,7 @@ def extras(device, flush, hbm, tf_sus, only=None, iters=None):
         raise SystemExit(f"unknown extra {only!r}; one of {sorted(runners)}")
     res = {}
     for name, fn in runners.items():
-        if only is not None and name != only:
+        if (only is not None and name != only) or name in skip:
             continue
         res[name] = fn()
         torch.cuda.empty_cache()
@@ -793,8 +843,7 @@ def run_reference(args, world):
         "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; reference recipe)",
-        "config": {"workload": args.workload, "batch": p.batch, "seqlen": p.seqlen,
-                   "d_inner": p.dim, "d_state": p.dstate, "io": p.io},
+        "config": bench_config(args.workload, p, world),
         "cpu_baseline": {"value": value, "unit": "state-updates/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "state-updates/s", "h2d_bytes_per_step": 0,
@@ -809,7 +858,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(k for k in WORKLOADS if k.startswith("scan")),
-                    default="scan_bf16_B8_D1536_L2048_N16")
+                    default="scan_bf16_B1_D2048_L131072_N16")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only-extra", default=None,

@@ -225,7 +225,11 @@ SSM_API ssm_status ssm_ssd_plan(const ssm_ssd_args *args, int32_t *tensor_core);
  *   A : (D, N) fp32                    D, delta_bias : (D) fp32
  * Nullable: D, delta_bias, z.  One call advances every sequence by one token;
  * calls on one stream are ordered, so L calls equal one ssm_scan_fwd over L steps
- * (up to rounding) with the same discretization.  No workspace. */
+ * (up to rounding) with the same discretization.
+ * workspace (optional): a 256-byte device status word, read with
+ * ssm_read_device_status; the bulk-copy kernel (N a multiple of 8 up to 64, 16-byte
+ * aligned rows) writes SSM_ERR_TIMEOUT there if one of its bounded waits gives up
+ * (without a workspace such a timeout goes unreported).  The call clears it first. */
 typedef struct {
     int64_t batch, dim, dstate;
     int32_t io_dtype;
@@ -236,6 +240,8 @@ typedef struct {
     void *y;
     int32_t discretization; /* ssm_discretization */
     int32_t reserved;       /* 0 */
+    void *workspace;        /* nullable; if given, >= 256 bytes, 256-byte aligned */
+    size_t workspace_bytes;
 } ssm_decode_args;
 
 SSM_API ssm_status ssm_step_decode(const ssm_decode_args *args, ssm_stream_t stream);

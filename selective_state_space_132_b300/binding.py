@@ -51,7 +51,8 @@ class DecodeArgs(ctypes.Structure):
                 ("io_dtype", _i32), ("delta_softplus", _i32), ("state", _fp),
                 ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp), ("z", _vp),
                 ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("y", _vp),
-                ("discretization", _i32), ("reserved", _i32)]
+                ("discretization", _i32), ("reserved", _i32),
+                ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class ScanBwdArgs(ctypes.Structure):
@@ -445,9 +446,12 @@ def step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: to
                 B: torch.Tensor, C: torch.Tensor, D: Optional[torch.Tensor] = None,
                 z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
                 delta_softplus: bool = True, y: Optional[torch.Tensor] = None,
-                stream=None, discretization: str = "euler") -> torch.Tensor:
+                stream=None, discretization: str = "euler",
+                workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """One recurrent step; ``state`` (B, D, N) fp32 is updated in place.
-    x, delta, z: (B, D); B, C: (B, N); A: (D, N) fp32; D, delta_bias: (D,) fp32."""
+    x, delta, z: (B, D); B, C: (B, N); A: (D, N) fp32; D, delta_bias: (D,) fp32.
+    workspace: optional 256-byte uint8 tensor that receives the device status word
+    (read it with read_device_status)."""
     lib = load_library()
     nb, Dm, N = state.shape
     dev, io = x.device, x.dtype
@@ -468,6 +472,9 @@ def step_decode(state: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: to
                       _ptr(delta), _ptr(B), _ptr(C), _ptr(z), _ptr(A), _ptr(D),
                       _ptr(delta_bias), _ptr(y))
     args.discretization = _disc(discretization)
+    if workspace is not None:
+        args.workspace = _ptr(workspace)
+        args.workspace_bytes = workspace.numel() * workspace.element_size()
     _launch(lib.ssm_step_decode, args, stream, x.device, "ssm_step_decode")
     return y
 

@@ -49,6 +49,7 @@ struct DecodeParams {
     const void *x, *delta, *Bm, *Cm, *z;
     const float *A, *Dv, *bias;
     void *y;
+    void *status;       // DeviceStatus (nullable)
 };
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t stream);
 

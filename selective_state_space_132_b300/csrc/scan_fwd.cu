@@ -365,17 +365,20 @@ void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64
     } else {
         // Each extra chunk costs a summary pass over that chunk (most of a scan of it),
         // so the sequence is split only when its chains alone cannot fill the GPU.
-        //  * TMA kernel: the largest split whose grid still fits in one wave of
-        //    resident blocks (measured on the long-context shape: 5 chunks 3.74 ms,
-        //    9 chunks (one full wave) 2.86 ms, 12 chunks (1.3 waves) 3.03 ms); the
-        //    130M-layer shape (384 blocks, 592 slots) stays whole.
+        //  * TMA kernel: a grid of at least half a wave of resident blocks is left
+        //    whole (the 130M-layer shape, 384 blocks for 592 slots: 200 us whole,
+        //    250-262 us split 2-8 ways).  A smaller grid is split into about six waves
+        //    of blocks, so that the last wave's tail is short (long-context shape, 64
+        //    blocks per chunk: 9 chunks (one wave) 2.85 ms, 32 chunks 2.66 ms, 64
+        //    chunks 2.65 ms).
         //  * general kernel: about eight warps per SM.
         // Chunks stay at least 1024 steps long.
         int64_t k;
         if (tma_blocks_per_sm > 0) {
             const int64_t per_chunk = batch * ((dim + 31) / 32);
             const int64_t slots = static_cast<int64_t>(device_sm_count()) * tma_blocks_per_sm;
-            k = per_chunk > 0 ? slots / per_chunk : 1;
+            k = (per_chunk <= 0 || 2 * per_chunk >= slots) ? 1
+                                                           : (6 * slots + per_chunk - 1) / per_chunk;
         } else {
             const int64_t warps = batch * ((dim + kDT - 1) / kDT) * lanes_for(dstate);
             const int64_t target = static_cast<int64_t>(device_sm_count()) * 8;

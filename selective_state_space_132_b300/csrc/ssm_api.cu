@@ -175,6 +175,10 @@ ssm_status check_decode(const ssm_decode_args *a) {
     if (overlaps(a->y, tok, a->x, tok) || overlaps(a->y, tok, a->delta, tok) ||
         overlaps(a->y, tok, a->z, tok) || overlaps(a->y, tok, a->state, st))
         return SSM_ERR_INVALID_ARG;
+    if (a->workspace) {
+        if (a->workspace_bytes < ssm::kStatusBytes) return SSM_ERR_WORKSPACE;
+        if (!aligned(a->workspace, 256)) return SSM_ERR_ALIGNMENT;
+    }
     return SSM_OK;
 }
 
@@ -423,7 +427,11 @@ ssm_status ssm_step_decode(const ssm_decode_args *a, ssm_stream_t stream) {
     p.Dv = a->D;
     p.bias = a->delta_bias;
     p.y = a->y;
-    return from_cuda(ssm::launch_decode(p, reinterpret_cast<cudaStream_t>(stream)));
+    p.status = a->workspace;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (a->workspace && cudaMemsetAsync(a->workspace, 0, ssm::kStatusBytes, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return from_cuda(ssm::launch_decode(p, st));
 }
 
 ssm_status ssm_ssd_step_decode(const ssm_ssd_decode_args *a, ssm_stream_t stream) {

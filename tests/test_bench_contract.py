@@ -24,7 +24,11 @@ def test_bench_prints_contract_line():
         assert key in d, key
     assert d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3
     assert d["value"] > 0 and d["ms_per_step"] > 0
-    assert d["gpu_launches"] == 5
+    # one or two launches per step (the long-context headline adds a summary pass)
+    import selective_state_space_132_b300 as ssm
+    c = d["config"]
+    per_call = ssm.scan_launches_per_call(c["batch"], c["seqlen"], c["d_inner"], c["d_state"])
+    assert d["gpu_launches"] == 5 * per_call
     r = d["roofline"]
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0 < r["frac"] < 1.5
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
