@@ -41,12 +41,16 @@ HBM_FALLBACK_GBS = 6400.0
 BF16_FALLBACK_TFLOPS = 1800.0
 L2_FLUSH_BYTES = 256 << 20
 
-# ncu DRAM traffic (bytes) per launch of the dominant kernel, keyed by the sha256
-# prefix of the kernel's sources at the time of the capture; an entry whose key no
+# ncu DRAM traffic (bytes, read + written) of one scan call (the summary pass and the
+# output pass when the plan splits the sequence), keyed by the sha256 prefix of the
+# kernel's sources at the time of the capture and by workload; an entry whose key no
 # longer matches the sources is ignored (traffic reported as null).
 PROFILED_TRAFFIC = {
-    # scan_tma_kernel, 130M-layer workload: 152,182,784 B read + 31,574,272 B written
-    "6a8e695b093e398a": 183757056,
+    "37f794e55ead3f6d": {
+        # summary pass 1,072.6 MB read + 6.6 MB written; output pass 1,683.8 MB read +
+        # 518.5 MB written (profiles/scan_tma_bf16_B1_D2048_L131072_N16.md)
+        "scan_bf16_B1_D2048_L131072_N16": 3281500000,
+    },
 }
 
 WORKLOADS = {
@@ -652,7 +656,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded; reference recipe)",
         "config": bench_config(args.workload, p, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": PROFILED_TRAFFIC.get(src_hash),
+                     "frac": achieved / hbm, "traffic": PROFILED_TRAFFIC.get(src_hash, {}).get(args.workload),
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": algo,
                      "frac_of_nominal_8000": achieved / 8000.0, "source_hash": src_hash},
         "gpu_launches": launches * args.steps,
