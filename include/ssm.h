@@ -81,11 +81,18 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
  * B, L or D of zero is valid; then only h_final (= h0, or zeros) is written.
  * time_chunk: 0 lets the library choose how many time steps one thread block walks;
  * a positive value (a multiple of 32) forces it, which splits long sequences over
- * several blocks joined by a carry pass (exact up to rounding).
+ * several blocks joined by a carry (exact up to rounding): each block of a later time
+ * chunk folds the end states of the earlier chunks of its channels, computed from a
+ * zero state (tildalice review, section "2. 병렬 스캔": the associative combine over
+ * whole chunks).  The TMA kernel does this in one launch, each block publishing its
+ * chunk's summary with a release store and acquiring its predecessors' with a bounded
+ * wait (SSM_ERR_TIMEOUT in the status word if one ever gave up); the general kernel in
+ * two (a summary pass, then the output pass).
  * Workspace: ssm_scan_workspace_size() bytes (it reads only the sizes and flags of
  * `args`, not the pointers), 256-byte aligned, always required: its first 256 bytes
- * hold the device status word (cleared by the call itself), the rest the chunk
- * summaries of a time-split sequence; contents need no initialisation.
+ * hold the device status word, the rest the chunk summaries and the hand-over flags of
+ * a time-split sequence; the call clears what must start at zero, so the contents need
+ * no initialisation.
  * discretization: SSM_DISC_EULER (0, B̄ = dl B: the simplified form of the tildalice
  * review, section "Δ의 직관적 이해") or SSM_DISC_ZOH (1, zero-order hold:
  * B̄ = (exp(dl A) - 1) / A B, section "이산화"; the A -> 0 limit is dl B). */
@@ -108,7 +115,7 @@ typedef struct {
 SSM_API ssm_status ssm_scan_workspace_size(const ssm_scan_args *args, size_t *bytes);
 /* How ssm_scan_fwd will run these sizes (reads sizes and flags only): the time
  * steps per chunk, the number of chunks along time, and the kernel launches per
- * call (1 when the sequence is one chunk, 2 when a summary pass is needed). */
+ * call (1, or 2 when a split sequence runs on the general kernel's summary pass). */
 SSM_API ssm_status ssm_scan_plan(const ssm_scan_args *args, int64_t *chunk_len,
                                  int32_t *nchunks, int32_t *launches);
 SSM_API ssm_status ssm_scan_fwd(const ssm_scan_args *args, ssm_stream_t stream);
@@ -314,6 +321,17 @@ SSM_API ssm_status ssm_read_device_status(const void *workspace, ssm_stream_t st
  * usable.  Asynchronous on `stream`. */
 SSM_API ssm_status ssm_check_bounded_wait(void *workspace, int64_t budget_cycles,
                                           ssm_stream_t stream);
+
+/* Diagnostic, no counterpart in the pages.  Runs ssm_scan_fwd's single-launch form
+ * (a sequence the TMA kernel splits over time chunks; otherwise SSM_ERR_UNSUPPORTED)
+ * with the chunk summaries left unpublished and a wait budget of `budget_cycles` SM
+ * clock cycles (1 .. 2e9).  The blocks of every chunk after the first wait for a
+ * predecessor that never publishes, give up after the budget, record SSM_ERR_TIMEOUT in
+ * the status word at the start of args->workspace and return without writing their
+ * outputs; the CUDA context stays usable.  Arguments and workspace as ssm_scan_fwd.
+ * Asynchronous on `stream`. */
+SSM_API ssm_status ssm_check_scan_lookback(const ssm_scan_args *args, int64_t budget_cycles,
+                                           ssm_stream_t stream);
 
 #ifdef __cplusplus
 }

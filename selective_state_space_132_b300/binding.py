@@ -20,7 +20,7 @@ EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_sca
             "ssm_scan_bwd_workspace_size", "ssm_scan_bwd",
             "ssm_ssd_workspace_size", "ssm_ssd_chunk_fwd", "ssm_ssd_plan", "ssm_step_decode",
             "ssm_ssd_step_decode", "ssm_conv1d", "ssm_status_string", "ssm_version",
-            "ssm_check_bounded_wait",
+            "ssm_check_bounded_wait", "ssm_check_scan_lookback",
             "ssm_read_device_status"]
 
 _i64, _i32, _vp, _fp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p
@@ -140,6 +140,8 @@ def load_library():
     lib.ssm_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
     lib.ssm_check_bounded_wait.argtypes = [_vp, ctypes.c_int64, _vp]
     lib.ssm_check_bounded_wait.restype = ctypes.c_int
+    lib.ssm_check_scan_lookback.argtypes = [ctypes.POINTER(ScanArgs), ctypes.c_int64, _vp]
+    lib.ssm_check_scan_lookback.restype = ctypes.c_int
     for fn in ("ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
                "ssm_ssd_workspace_size", "ssm_ssd_chunk_fwd", "ssm_ssd_plan", "ssm_step_decode",
                "ssm_read_device_status"):

@@ -111,6 +111,9 @@ struct DeviceStatus {
     int32_t pad[62];
 };
 constexpr size_t kStatusBytes = 256;
+// Clock budget of a block waiting for the chunk summaries of its predecessors in the
+// single-launch scan (about one second at 2 GHz).
+constexpr long long kScanWaitCycles = 2000000000LL;
 
 __device__ __forceinline__ void report_status(DeviceStatus *st, int code, int where) {
     if (st) {

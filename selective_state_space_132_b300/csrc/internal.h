@@ -23,6 +23,12 @@ struct ScanParams {
     void *status;       // DeviceStatus at the start of the workspace (may be null)
     int clear_status;   // the first block of this launch clears the status word
     int zoh;            // 1: zero-order-hold input coefficient instead of dl
+    // single-launch carry (TMA kernel, nchunks > 1): a block ticket and one flag per
+    // (batch row, chunk, 32-channel slab), zeroed by the caller; null: two launches
+    uint32_t *ticket;
+    uint32_t *flags;
+    long long wait_budget;  // clock cycles a block may wait for its predecessors
+    int publish;            // 0 only in the look-back self-test: summaries stay unpublished
 };
 
 // TMA-staged scan (scan_tma.cu): warps per 32-channel block for these sizes (0 = the
@@ -38,6 +44,10 @@ cudaError_t launch_scan_tma(const ScanParams &p, cudaStream_t stream);
 void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t time_chunk,
                int tma_blocks_per_sm, int64_t *chunk_len, int *nchunks);
 size_t scan_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, int nchunks);
+// Byte offset and size of the look-back ticket and flags inside a scan workspace (zero
+// size when the call needs none).
+void scan_lookback_region(int64_t batch, int64_t dim, int64_t dstate, int nchunks,
+                          size_t *offset, size_t *bytes);
 cudaError_t launch_scan(const ScanParams &p, cudaStream_t stream);
 
 struct DecodeParams {

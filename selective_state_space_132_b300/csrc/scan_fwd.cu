@@ -394,13 +394,27 @@ void scan_plan(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64
     *nchunks = static_cast<int>(std::max<int64_t>(1, k));
 }
 
+// Workspace: the device status word, then (when the sequence is split) the chunk end
+// states (B, K, D, N) and step sums (B, K, D), then the look-back ticket and flags
+// (1 + B K ceil(D / 32) words), each part on a 256-byte boundary.
+void scan_lookback_region(int64_t batch, int64_t dim, int64_t dstate, int nchunks,
+                          size_t *offset, size_t *bytes) {
+    *offset = 0;
+    *bytes = 0;
+    if (nchunks <= 1) return;
+    const size_t rows = static_cast<size_t>(batch) * nchunks * dim;
+    *offset = kStatusBytes + (rows * dstate * sizeof(float) + 255) / 256 * 256 +
+              (rows * sizeof(float) + 255) / 256 * 256;
+    const size_t words = 1 + static_cast<size_t>(batch) * nchunks * ((dim + 31) / 32);
+    *bytes = (words * 4 + 255) / 256 * 256;
+}
+
 size_t scan_workspace_bytes(int64_t batch, int64_t dim, int64_t dstate, int nchunks) {
     size_t bytes = kStatusBytes;  // device status word
     if (nchunks > 1) {
-        const size_t rows = static_cast<size_t>(batch) * nchunks * dim;
-        const size_t hl = rows * dstate * sizeof(float);
-        bytes += (hl + 255) / 256 * 256;
-        bytes += (rows * sizeof(float) + 255) / 256 * 256;
+        size_t off, lb;
+        scan_lookback_region(batch, dim, dstate, nchunks, &off, &lb);
+        bytes = off + lb;
     }
     return bytes;
 }

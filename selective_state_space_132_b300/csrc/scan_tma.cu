@@ -59,12 +59,23 @@ constexpr int kStages = SSM_SCAN_STAGES;  // TMA pipeline depth
 #define SSM_SCAN_UNROLL 4
 #endif
 constexpr int kU = SSM_SCAN_UNROLL;  // time steps per ILP block of the scan loop
+#ifndef SSM_SCAN_LOOKBACK
+#define SSM_SCAN_LOOKBACK 1
+#endif
+// a sequence split over time chunks runs in one launch (look-back carry) or two
+constexpr bool kScanLookback = SSM_SCAN_LOOKBACK != 0;
+#ifndef SSM_SCAN_SPLIT_RED
+#define SSM_SCAN_SPLIT_RED 1
+#endif
+// the output pass of a split sequence adds the partial readouts of a channel's lanes
+// with shuffles (smaller shared memory, more resident blocks)
+constexpr bool kSplitRed = SSM_SCAN_SPLIT_RED != 0;
 
 __host__ __device__ constexpr int align1k(int v) { return (v + 1023) / 1024 * 1024; }
 
 // Shared-memory layout of one block: WPC warps, each owning CPW = 32 / LPC channels;
 // the block's CPB = WPC * CPW channels form one token-tile row of ROWB bytes.
-template <typename TIO, int NS, int LPC, int WPC, bool kSummary> struct Layout {
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kRed = false> struct Layout {
     static constexpr int CPW = 32 / LPC;
     static constexpr int CPB = CPW * WPC;
     static constexpr int N = NS * LPC;
@@ -90,11 +101,14 @@ template <typename TIO, int NS, int LPC, int WPC, bool kSummary> struct Layout {
     static constexpr int kDlxRow = 2 * kT + 4;
     static constexpr int o_dlx = kStages * stage;
     // per warp: LPC slots of partial readouts [slot][t][channel], t-stride CPW + 4
-    // (conflict-free row reads) and slot stride = 8 mod 32 (conflict-free writes)
+    // (conflict-free row reads) and slot stride = 8 mod 32 (conflict-free writes);
+    // with kRed the LPC lanes of a channel add their partials with shuffles first and
+    // one slot holds the sums (a quarter of the shared memory, more blocks per SM)
+    static constexpr int kSlots = kRed ? 1 : LPC;
     static constexpr int kPartT = CPW + 4;
     static constexpr int kPart = (kT * kPartT + 31) / 32 * 32 + 8;
     static constexpr int o_part = o_dlx + align1k(CPB * kDlxRow * 4);
-    static constexpr int o_y = o_part + (kSummary ? 0 : align1k(WPC * LPC * kPart * 4));
+    static constexpr int o_y = o_part + (kSummary ? 0 : align1k(WPC * kSlots * kPart * 4));
     static constexpr int o_bar = o_y + (kSummary ? 0 : 2 * align1k(kTok));
     static constexpr int bytes = o_bar + kStages * 8 + 1024;  // + slack to align the base
 };
@@ -150,10 +164,18 @@ template <bool kFast> __device__ __forceinline__ f2 decay2(float dl, f2 a) {
     return f2{expf(v.x), expf(v.y)};
 }
 
-template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh>
-__global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constant__ TmaMaps maps,
-                                                            ScanParams p) {
-    using LY = Layout<TIO, NS, LPC, WPC, kSummary>;
+// One pass over chunk c of batch row b for the block's channel slab (channels d0 ..
+// d0 + CPB - 1): the summary pass (kSummary: from a zero state, keeping the chunk's end
+// state and step sum) or the output pass (from h0 folded through the summaries of the
+// chunks before c).  kLB selects the single-launch form: the output pass first acquires
+// the summaries of the earlier chunks (each published by its block with a release
+// store) and the summary pass publishes its own.  Returns false after a bounded wait
+// gave up (the status word then says so).
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kLB,
+          bool kRed>
+__device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams &p, int b,
+                                           int c, int d0, int slab) {
+    using LY = Layout<TIO, NS, LPC, WPC, kSummary, kRed>;
     using CK = Chunk<TIO>;
     constexpr int CPW = LY::CPW, CPB = LY::CPB, N = LY::N, ROWB = LY::ROWB;
     constexpr int EC = CK::EC;                  // elements per 16-byte chunk
@@ -172,17 +194,10 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
     const int warp = tid >> 5, lane = tid & 31;
     const int64_t D = p.dim, L = p.seqlen;
     const int K = p.nchunks;
-    const int b = blockIdx.y;
-    const int c = blockIdx.z;
-    const int d0 = blockIdx.x * CPB;
     const bool has_z = p.z != nullptr;
     DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
-    float *part = reinterpret_cast<float *>(smem + LY::o_part) + warp * LPC * LY::kPart;
-
-    // the first block of the first launch of a call clears the status word
-    if (p.clear_status && status && tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
-        blockIdx.z == 0)
-        status->code = 0;
+    float *part = reinterpret_cast<float *>(smem + LY::o_part) + warp * LY::kSlots * LY::kPart;
+    const int nslabs = static_cast<int>((D + CPB - 1) / CPB);
 
     const int64_t t_begin = static_cast<int64_t>(c) * p.chunk_len;
     const int64_t t_end = min(L, t_begin + p.chunk_len);
@@ -193,6 +208,37 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
         ptx::fence_mbar_init();
     }
     __syncthreads();
+    // the barriers are invalidated when the pass ends, so that the block's next pass
+    // can reuse their shared memory
+    auto release_barriers = [&]() {
+        __syncthreads();
+        if (tid == 0)
+            for (int s = 0; s < kStages; ++s) ptx::mbar_inval(&bars[s]);
+        __syncthreads();
+    };
+    if (kLB && !kSummary && c > 0) {
+        // acquire the summaries of chunks 0 .. c - 1 of this slab (their blocks took
+        // earlier tickets, so they have started and publish before they wait on anything)
+        int late = 0;
+        if (tid == 0) {
+            const long long t0 = clock64();
+            for (int cc = 0; cc < c && !late; ++cc) {
+                const uint32_t *f = p.flags + (static_cast<int64_t>(b) * K + cc) * nslabs + slab;
+                while (ptx::ld_acquire_u32(f) == 0u) {
+                    if (clock64() - t0 > p.wait_budget) {
+                        late = 1;
+                        break;
+                    }
+                    __nanosleep(128);
+                }
+            }
+        }
+        if (__syncthreads_or(late)) {
+            if (tid == 0) report_status(status, SSM_ERR_TIMEOUT, 13);
+            release_barriers();
+            return false;  // nothing was issued yet
+        }
+    }
 
     auto issue = [&](int tile) {  // thread 0 only
         const int s = tile % kStages;
@@ -238,11 +284,11 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
         // fold the summaries of the chunks before this one into the initial state
         for (int cc = 0; cc < c; ++cc) {
             const int64_t row = (static_cast<int64_t>(b) * K + cc) * D + sd;
-            const float S = sdval ? p.dsum[row] : 0.f;
+            const float S = sdval ? __ldcg(p.dsum + row) : 0.f;
 #pragma unroll
             for (int k = 0; k < NS / 2; ++k) {
                 const int n = j * NS + 2 * k;
-                const f2 he = sdval ? f2{p.hloc[row * N + n], p.hloc[row * N + n + 1]}
+                const f2 he = sdval ? f2{__ldcg(p.hloc + row * N + n), __ldcg(p.hloc + row * N + n + 1)}
                                     : f2{0.f, 0.f};
                 h[k] = ptx::fma2(decay2<kFast>(S, a2[k]), h[k], he);
             }
@@ -390,10 +436,21 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
                     acc[u] = s2.x + s2.y;
                     if (kSummary) dsum += dl[u];
                 }
-                if (!kSummary) {
+                if (!kSummary && !kRed) {
 #pragma unroll
                     for (int u = 0; u < kU; ++u)
                         part[j * LY::kPart + (tb + u) * LY::kPartT + sc] = acc[u];
+                }
+                if (!kSummary && kRed) {
+                    // sum over the channel's LPC adjacent lanes; lane slot j then stores
+                    // the steps u with u % LPC == j
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+#pragma unroll
+                        for (int m = 1; m < LPC; m <<= 1)
+                            acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], m);
+                        if (u % LPC == j) part[(tb + u) * LY::kPartT + sc] = acc[u];
+                    }
                 }
             }
         }
@@ -407,7 +464,7 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
             for (int cc = 0; cc < CPW; cc += 4) {
                 float4 a4 = *reinterpret_cast<const float4 *>(part + lane * LY::kPartT + cc);
 #pragma unroll
-                for (int jj = 1; jj < LPC; ++jj) {
+                for (int jj = 1; jj < LY::kSlots; ++jj) {
                     const float4 v = *reinterpret_cast<const float4 *>(
                         part + jj * LY::kPart + lane * LY::kPartT + cc);
                     const f2 lo = ptx::add2(f2{a4.x, a4.y}, f2{v.x, v.y});
@@ -452,6 +509,8 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
         // released (each wait again bounded)
         for (int i = failed_tile; i < failed_tile + kStages && i < ntiles; ++i)
             if (!ptx::mbar_wait(&bars[i % kStages], (i / kStages) & 1)) break;
+        if (!kSummary && tid == 0) ptx::bulk_wait<0>();
+        return false;
     }
     if (!kSummary && tid == 0) ptx::bulk_wait<0>();
 
@@ -466,6 +525,13 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
             // every lane of the channel accumulated the same sum; one writes it
             if (j == 0) p.dsum[row] = dsum;
         }
+        if (kLB) {
+            // publish: the block's summary writes happen before the flag's release
+            __threadfence();
+            __syncthreads();
+            if (tid == 0 && p.publish)
+                ptx::st_release_u32(p.flags + (static_cast<int64_t>(b) * K + c) * nslabs + slab, 1u);
+        }
     } else if (c == K - 1 && p.h_final && sdval) {
 #pragma unroll
         for (int k = 0; k < NS / 2; ++k) {
@@ -474,14 +540,58 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
                 make_float2(h[k].x, h[k].y);
         }
     }
+    release_barriers();
+    return true;
+}
+
+// Two-launch form: the summary pass over chunks 0 .. K-2, then the output pass.
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kRed>
+__global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constant__ TmaMaps maps,
+                                                            ScanParams p) {
+    using LY = Layout<TIO, NS, LPC, WPC, kSummary, kRed>;
+    DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
+    // the first block of the first launch of a call clears the status word
+    if (p.clear_status && status && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
+        blockIdx.z == 0)
+        status->code = 0;
+    (void)chunk_pass<TIO, NS, LPC, WPC, kSummary, kZoh, false, kRed>(
+        maps, p, blockIdx.y, blockIdx.z, blockIdx.x * LY::CPB, blockIdx.x);
+}
+
+// Single-launch form with a decoupled look-back.  Blocks take their work from an atomic
+// ticket in chunk-major order (every slab of chunk 0, then of chunk 1, ...): a block
+// scans its chunk from a zero state and publishes the summary (all chunks but the last),
+// then acquires the summaries of the earlier chunks of its slab, folds them into its
+// initial state and runs the output pass.  A block waits only on blocks with smaller
+// tickets, which have started and publish before they wait themselves, so the waits end;
+// they are bounded all the same.  Every chunk but the last is still read twice (summary
+// and output), as in the two-launch form; what goes is the launch boundary between the
+// passes and the idle tail of the first launch.
+template <typename TIO, int NS, int LPC, int WPC, bool kZoh, bool kRed>
+__global__ void __launch_bounds__(32 * WPC) scan_tma_lb_kernel(const __grid_constant__ TmaMaps maps,
+                                                               ScanParams p) {
+    using LY = Layout<TIO, NS, LPC, WPC, false, kRed>;
+    __shared__ int s_ticket;
+    if (threadIdx.x == 0) s_ticket = static_cast<int>(atomicAdd(p.ticket, 1u));
+    __syncthreads();
+    const int ticket = s_ticket;
+    const int nslabs = static_cast<int>((p.dim + LY::CPB - 1) / LY::CPB);
+    const int per_chunk = static_cast<int>(p.batch) * nslabs;
+    const int c = ticket / per_chunk, r = ticket % per_chunk;
+    const int b = r / nslabs, slab = r % nslabs;
+    if (c < p.nchunks - 1 &&
+        !chunk_pass<TIO, NS, LPC, WPC, true, kZoh, true, kRed>(maps, p, b, c, slab * LY::CPB, slab))
+        return;
+    (void)chunk_pass<TIO, NS, LPC, WPC, false, kZoh, true, kRed>(maps, p, b, c, slab * LY::CPB,
+                                                                   slab);
 }
 
 // ---------------------------------------------------------------- host side
-template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh>
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kRed>
 cudaError_t launch_tma_one(const ScanParams &p, const TmaMaps &maps, int nchunks_grid,
                            cudaStream_t stream) {
-    using LY = Layout<TIO, NS, LPC, WPC, kSummary>;
-    auto kern = scan_tma_kernel<TIO, NS, LPC, WPC, kSummary, kZoh>;
+    using LY = Layout<TIO, NS, LPC, WPC, kSummary, kRed>;
+    auto kern = scan_tma_kernel<TIO, NS, LPC, WPC, kSummary, kZoh, kRed>;
     if (LY::bytes > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              LY::bytes);
@@ -509,13 +619,28 @@ cudaError_t launch_tma_pair(ScanParams p, cudaStream_t stream) {
     if (ok && p.z) ok = make_tma_map_3d(&m.z, p.z, bf, B, L, D, LY::CPB, kT, LY::ROWB);
     if (!ok) return cudaErrorInvalidValue;
     p.clear_status = 1;
+    if (p.nchunks > 1 && p.flags && kScanLookback) {
+        // one launch, the chunk summaries handed over through the look-back flags (the
+        // caller zeroed the status word, the ticket and the flags)
+        using LR = Layout<TIO, NS, LPC, WPC, false, kSplitRed>;
+        auto kern = scan_tma_lb_kernel<TIO, NS, LPC, WPC, kZoh, kSplitRed>;
+        if (LR::bytes > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 LR::bytes);
+            if (e != cudaSuccess) return e;
+        }
+        const int64_t blocks = static_cast<int64_t>(p.nchunks) * p.batch * ((D + LR::CPB - 1) / LR::CPB);
+        kern<<<static_cast<unsigned>(blocks), 32 * WPC, LR::bytes, stream>>>(m, p);
+        return cudaGetLastError();
+    }
     if (p.nchunks > 1) {
         cudaError_t e =
-            launch_tma_one<TIO, NS, LPC, WPC, true, kZoh>(p, m, p.nchunks - 1, stream);
+            launch_tma_one<TIO, NS, LPC, WPC, true, kZoh, false>(p, m, p.nchunks - 1, stream);
         if (e != cudaSuccess) return e;
         p.clear_status = 0;
+        return launch_tma_one<TIO, NS, LPC, WPC, false, kZoh, kSplitRed>(p, m, p.nchunks, stream);
     }
-    return launch_tma_one<TIO, NS, LPC, WPC, false, kZoh>(p, m, p.nchunks, stream);
+    return launch_tma_one<TIO, NS, LPC, WPC, false, kZoh, false>(p, m, p.nchunks, stream);
 }
 
 }  // namespace

@@ -330,12 +330,20 @@ ssm_status ssm_scan_plan(const ssm_scan_args *a, int64_t *chunk_len, int32_t *nc
     scan_ws(a, &cl, &k);
     *chunk_len = cl;
     *nchunks = k;
-    *launches = (a->batch == 0 || a->dim == 0) ? 0 : (k > 1 ? 2 : 1);
+    // the TMA kernel runs a split sequence in one launch (look-back carry), the general
+    // kernel in two (summary pass, output pass)
+    const bool tma = ssm::scan_tma_sizes_ok(a->io_dtype == SSM_BF16, a->seqlen, a->dim, a->dstate);
+    *launches = (a->batch == 0 || a->dim == 0) ? 0 : (k > 1 && !tma ? 2 : 1);
     return SSM_OK;
 }
 
-ssm_status ssm_scan_fwd(const ssm_scan_args *a, ssm_stream_t stream) {
-    NvtxRange nvtx("ssm_scan_fwd");
+}  // extern "C"
+
+namespace {
+// The scan call; `budget` and `publish` differ from the defaults only in the look-back
+// self-test.
+ssm_status scan_fwd_impl(const ssm_scan_args *a, ssm_stream_t stream, long long budget,
+                         int publish) {
     ssm_status s = check_scan(a);
     if (s != SSM_OK) return s;
     int64_t cl;
@@ -366,13 +374,47 @@ ssm_status ssm_scan_fwd(const ssm_scan_args *a, ssm_stream_t stream) {
     p.nchunks = k;
     p.status = a->workspace;
     p.zoh = a->discretization == SSM_DISC_ZOH;
+    p.wait_budget = budget;
+    p.publish = publish;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the status word starts at zero
+    if (cudaMemsetAsync(a->workspace, 0, kStatusBytes, st) != cudaSuccess) return SSM_ERR_CUDA;
     if (k > 1) {
         char *ws = static_cast<char *>(a->workspace) + kStatusBytes;
         const size_t rows = (size_t)a->batch * k * a->dim;
         p.hloc = reinterpret_cast<float *>(ws);
         p.dsum = reinterpret_cast<float *>(ws + (rows * a->dstate * sizeof(float) + 255) / 256 * 256);
+        size_t off, lb;
+        ssm::scan_lookback_region(a->batch, a->dim, a->dstate, k, &off, &lb);
+        // so do the look-back ticket and flags
+        if (cudaMemsetAsync(static_cast<char *>(a->workspace) + off, 0, lb, st) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        p.ticket = reinterpret_cast<uint32_t *>(static_cast<char *>(a->workspace) + off);
+        p.flags = p.ticket + 1;
     }
-    return from_cuda(ssm::launch_scan(p, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(ssm::launch_scan(p, st));
+}
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_scan_fwd(const ssm_scan_args *a, ssm_stream_t stream) {
+    NvtxRange nvtx("ssm_scan_fwd");
+    return scan_fwd_impl(a, stream, ssm::kScanWaitCycles, 1);
+}
+
+ssm_status ssm_check_scan_lookback(const ssm_scan_args *a, int64_t budget_cycles,
+                                   ssm_stream_t stream) {
+    if (budget_cycles < 1 || budget_cycles > ssm::kScanWaitCycles) return SSM_ERR_INVALID_ARG;
+    ssm_status s = check_scan(a);
+    if (s != SSM_OK) return s;
+    int64_t cl;
+    int k;
+    scan_ws(a, &cl, &k);
+    // only a split sequence on the TMA kernel waits on its predecessors
+    if (k < 2 || !ssm::scan_tma_sizes_ok(a->io_dtype == SSM_BF16, a->seqlen, a->dim, a->dstate))
+        return SSM_ERR_UNSUPPORTED;
+    return scan_fwd_impl(a, stream, budget_cycles, 0);
 }
 
 ssm_status ssm_ssd_workspace_size(const ssm_ssd_args *a, size_t *bytes) {
