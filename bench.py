@@ -46,10 +46,10 @@ L2_FLUSH_BYTES = 256 << 20
 # kernel's sources at the time of the capture and by workload; an entry whose key no
 # longer matches the sources is ignored (traffic reported as null).
 PROFILED_TRAFFIC = {
-    "37f794e55ead3f6d": {
-        # summary pass 1,072.6 MB read + 6.6 MB written; output pass 1,683.8 MB read +
-        # 518.5 MB written (profiles/scan_tma_bf16_B1_D2048_L131072_N16.md)
-        "scan_bf16_B1_D2048_L131072_N16": 3281500000,
+    "7dafdf4e062c9758": {
+        # scan_tma_lb_kernel (summary and output passes in one launch), mean of 5 calls:
+        # 3,210.2 MB read + 525.6 MB written (profiles/scan_tma_bf16_B1_D2048_L131072_N16.md)
+        "scan_bf16_B1_D2048_L131072_N16": 3735800000,
     },
 }
 
