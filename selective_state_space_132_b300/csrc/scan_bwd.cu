@@ -39,9 +39,13 @@ namespace {
 constexpr int kCB = 32;          // channels per block
 constexpr int kThreads = 128;
 
+#ifndef SSM_BWD_TILE_NS4
+#define SSM_BWD_TILE_NS4 16
+#endif
 template <int NS> struct BwdShape {
     static constexpr int NP = 4 * NS;                            // padded state count
-    static constexpr int T = NS <= 2 ? 32 : 64 / NS;             // steps per tile
+    // steps per tile (and between checkpoints)
+    static constexpr int T = NS <= 2 ? 32 : (NS == 4 ? SSM_BWD_TILE_NS4 : 64 / NS);
     static_assert(NS % 2 == 0, "states are processed in packed pairs");
     static constexpr int kRows = 9;                              // per-(t, channel) arrays
     static constexpr size_t floats = static_cast<size_t>(T) * kCB * NP   // states
