@@ -8,7 +8,9 @@ from typing import Optional, Tuple
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "libssm.so")
+# SSM_LIBRARY names another build of the same library (e.g. one compiled with different
+# tile switches); by default the in-tree build next to this file is loaded.
+_LIB_PATH = os.environ.get("SSM_LIBRARY") or os.path.join(_HERE, "libssm.so")
 _lib = None
 
 SSM_F32, SSM_BF16 = 0, 1

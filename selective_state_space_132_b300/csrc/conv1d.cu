@@ -172,15 +172,23 @@ __global__ void __launch_bounds__(kBlock) conv1d_kernel(Conv1dParams p) {
 // RPT = 4 consecutive rows of one 16-byte chunk from shared memory; the outputs go to a
 // double-buffered shared tile that one TMA store writes back.  The rows never pass
 // through the LSU queue of a thread, and the thread body is small.
+#ifndef SSM_CONV_TT
+#define SSM_CONV_TT 128
+#endif
+#ifndef SSM_CONV_STAGES
+#define SSM_CONV_STAGES 3
+#endif
 constexpr int kBlockT = 256;
-constexpr int kTT = 128;           // steps per tile
-constexpr int kStagesT = 3;
+constexpr int kTT = SSM_CONV_TT;   // steps per tile
+constexpr int kStagesT = SSM_CONV_STAGES;
 constexpr int kRowB = 128;         // bytes of channels per tile row
 constexpr int kStageB = ((kTT + kMaxK - 1) * kRowB + 1023) / 1024 * 1024;
 constexpr int kYB = kTT * kRowB;
 constexpr int kOffY = kStagesT * kStageB;
 constexpr int kOffBar = kOffY + 2 * kYB;
 constexpr int kTmaSmem = kOffBar + kStagesT * 8 + 1024;   // + slack to align the base
+static_assert(kTT % 32 == 0 && kTT + kMaxK - 1 <= 256, "a TMA box spans at most 256 steps");
+static_assert(kStagesT >= 2 && kTmaSmem <= 227 * 1024, "stages must fit in shared memory");
 
 struct Conv1dMaps {
     CUtensorMap x, y;
