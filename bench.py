@@ -541,9 +541,12 @@ def scan_bwd_bytes(nb, L, D, N, e, gate=True):
         + 2 * nb * L * N * 4 + 2 * D * N * 4 + 4 * D * 4
 
 
-def time_scan_bwd(p, flush, device, iters=10):
-    """Median time of one ssm_scan_bwd call (states recomputed) on the scan problem p,
-    including the zeroing of the summed gradients, L2 flushed before each call."""
+def time_scan_bwd(p, flush, device, iters=10, checkpoints=False):
+    """Median time of one ssm_scan_bwd call on the scan problem p, including the zeroing
+    of the summed gradients, L2 flushed before each call.  The states are recomputed:
+    from checkpoints of the kernel's own (default), or from the checkpoints a forward
+    call with checkpoints wrote (ssm_scan_bwd_ckpt); then also returns the median times
+    of that forward call and of the plain forward call."""
     import torch
     import selective_state_space_132_b300 as ssm
     t = _to_dev(device)
@@ -552,11 +555,28 @@ def time_scan_bwd(p, flush, device, iters=10):
     Bm, Cm = t(p.B, io), t(p.C, io)
     A, Dv, bias = t(p.A), t(p.D), t(p.bias)
     dy = torch.randn_like(x)
-    ws = torch.empty(ssm.scan_bwd_workspace_size(p.batch, p.seqlen, p.dim, p.dstate, io),
-                     dtype=torch.uint8, device=device)
-    return _median_event_time(
-        lambda: ssm.scan_bwd(dy, x, dl, A, Bm, Cm, D=Dv, z=z, delta_bias=bias, workspace=ws),
-        flush, iters)
+    if not checkpoints:
+        ws = torch.empty(ssm.scan_bwd_workspace_size(p.batch, p.seqlen, p.dim, p.dstate, io),
+                         dtype=torch.uint8, device=device)
+        return _median_event_time(
+            lambda: ssm.scan_bwd(dy, x, dl, A, Bm, Cm, D=Dv, z=z, delta_bias=bias,
+                                 workspace=ws), flush, iters)
+    ck = torch.empty(ssm.scan_ckpt_shape(p.batch, p.seqlen, p.dim, p.dstate),
+                     dtype=torch.float32, device=device)
+    y = torch.empty_like(x)
+    hf = torch.empty((p.batch, p.dim, p.dstate), dtype=torch.float32, device=device)
+
+    def fwd(with_ck):
+        ssm.scan_fwd(x, dl, A, Bm, Cm, D=Dv, z=z, delta_bias=bias, y=y, h_final=hf,
+                     checkpoints=ck if with_ck else None)
+    t_fwd_ck = _median_event_time(lambda: fwd(True), flush, iters)
+    t_fwd = _median_event_time(lambda: fwd(False), flush, iters)
+    fwd(True)
+    ws = torch.empty(256, dtype=torch.uint8, device=device)
+    t_bwd = _median_event_time(
+        lambda: ssm.scan_bwd(dy, x, dl, A, Bm, Cm, D=Dv, z=z, delta_bias=bias, workspace=ws,
+                             checkpoints=ck), flush, iters)
+    return t_bwd, t_fwd_ck, t_fwd, ck.numel() * 4
 
 
 def cpu_baseline_scan(p, target_s=10.0, max_s=30.0):
@@ -781,9 +801,16 @@ def extras(device, flush, hbm, tf_sus, only=None, iters=None, skip=()):
             lambda th: oracle.scan_bwd(gy, p.x[:1], p.delta[:1], p.A, p.B[:1], p.C[:1],
                                        Dv=p.D, z=p.z[:1], bias=p.bias, threads=th),
             p.seqlen * p.dim * p.dstate, "state-updates/s", "batch row 0 of 8")
+        sc, f_ck, f, ck_bytes = time_scan_bwd(p, flush, device, iters=n(10), checkpoints=True)
         return {"ms": s * 1e3, "updates_per_s": p.updates / s, "gbs": b / s / 1e9,
                 "hbm_frac": b / s / 1e9 / hbm,
                 "note": "states recomputed: a checkpoint pass and a reverse pass",
+                "from_forward_checkpoints": {
+                    "ms": sc * 1e3, "updates_per_s": p.updates / sc,
+                    "forward_with_checkpoints_ms": f_ck * 1e3, "forward_ms": f * 1e3,
+                    "checkpoint_bytes": ck_bytes,
+                    "note": "the forward call keeps the state every 16 steps and the "
+                            "backward starts from them (reverse pass only)"},
                 "oracle": orc}
 
     runners = {

@@ -165,6 +165,32 @@ typedef struct {
 SSM_API ssm_status ssm_scan_bwd_workspace_size(const ssm_scan_bwd_args *args, size_t *bytes);
 SSM_API ssm_status ssm_scan_bwd(const ssm_scan_bwd_args *args, ssm_stream_t stream);
 
+/* ------------------------------------------------------------------ state checkpoints
+ * No counterpart in the pages: an optional trade of memory for backward time.
+ * ssm_scan_bwd rebuilds the hidden states from checkpoints: the state before every
+ * step t with t % T == 0, T = 32 (N <= 8), 16 (N <= 16), 8 (N <= 32) or 4 (N <= 64),
+ * stored as a (B, ceil(L / T), D, N) fp32 tensor.  It computes them itself, in a
+ * forward pass over the sequence at the start of the call.  A caller that can keep
+ * them from its forward call to its backward call (L / T times the size of h_final)
+ * saves that pass:
+ *   - ssm_scan_ckpt_size: T and the bytes of the checkpoint tensor for the sizes of
+ *     `args` (reads sizes only).
+ *   - ssm_scan_fwd_ckpt: ssm_scan_fwd (same arguments, workspace and results), and
+ *     it also writes the checkpoints to `ckpt` (device memory, caller-owned, 16-byte
+ *     aligned, at least ssm_scan_ckpt_size bytes; SSM_ERR_INVALID_ARG when it is
+ *     smaller or missing).  The states are the scan's own, to rounding: a sequence the
+ *     scan splits over time holds the states folded through the chunk summaries.
+ *   - ssm_scan_bwd_ckpt: ssm_scan_bwd (same arguments and results), reading the
+ *     checkpoints from `ckpt` (as written by ssm_scan_fwd_ckpt for the same inputs)
+ *     instead of computing them; its workspace needs only the 256-byte status word.
+ *     Checkpoints of other inputs give wrong gradients, not an error. */
+SSM_API ssm_status ssm_scan_ckpt_size(const ssm_scan_args *args, int64_t *steps,
+                                      size_t *bytes);
+SSM_API ssm_status ssm_scan_fwd_ckpt(const ssm_scan_args *args, float *ckpt,
+                                     size_t ckpt_bytes, ssm_stream_t stream);
+SSM_API ssm_status ssm_scan_bwd_ckpt(const ssm_scan_bwd_args *args, const float *ckpt,
+                                     size_t ckpt_bytes, ssm_stream_t stream);
+
 /* ------------------------------------------------------------------ scan without allocation
  * No counterpart in the pages: a library convenience.  Same computation, arguments
  * and results as ssm_scan_fwd, but the scratch that a time-split sequence needs

@@ -17,15 +17,15 @@ in the library's kernels; if the library is missing, the calls raise.
 from __future__ import annotations
 
 from .binding import (SSMError, build_library, conv1d, library_path, load_library,
-                      read_device_status, scan_bwd, scan_bwd_workspace_size, scan_fwd,
-                      selective_scan,
+                      read_device_status, scan_bwd, scan_bwd_workspace_size, scan_ckpt_shape,
+                      scan_ckpt_steps, scan_fwd, selective_scan,
                       scan_fwd_noalloc, scan_launches_per_call, scan_plan, scan_workspace_size,
                       ssd_chunk_fwd, ssd_step_decode, ssd_uses_tensor_cores, ssd_workspace_size,
                       step_decode, version)
 
 __all__ = ["SSMError", "build_library", "conv1d", "library_path", "load_library",
-           "read_device_status", "scan_bwd", "scan_bwd_workspace_size", "scan_fwd",
-           "selective_scan",
+           "read_device_status", "scan_bwd", "scan_bwd_workspace_size", "scan_ckpt_shape",
+           "scan_ckpt_steps", "scan_fwd", "selective_scan",
            "scan_fwd_noalloc", "scan_launches_per_call", "scan_plan", "scan_workspace_size",
            "ssd_chunk_fwd", "ssd_step_decode", "ssd_uses_tensor_cores", "ssd_workspace_size",
            "step_decode", "version"]

@@ -20,6 +20,7 @@ _STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED",
 
 EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
             "ssm_scan_bwd_workspace_size", "ssm_scan_bwd",
+            "ssm_scan_ckpt_size", "ssm_scan_fwd_ckpt", "ssm_scan_bwd_ckpt",
             "ssm_ssd_workspace_size", "ssm_ssd_chunk_fwd", "ssm_ssd_plan", "ssm_step_decode",
             "ssm_ssd_step_decode", "ssm_conv1d", "ssm_status_string", "ssm_version",
             "ssm_check_bounded_wait", "ssm_check_scan_lookback",
@@ -137,6 +138,13 @@ def load_library():
     lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_int
     lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanBwdArgs), _vp]
     lib.ssm_scan_bwd.restype = ctypes.c_int
+    lib.ssm_scan_ckpt_size.argtypes = [ctypes.POINTER(ScanArgs), ctypes.POINTER(ctypes.c_int64),
+                                       ctypes.POINTER(ctypes.c_size_t)]
+    lib.ssm_scan_ckpt_size.restype = ctypes.c_int
+    lib.ssm_scan_fwd_ckpt.argtypes = [ctypes.POINTER(ScanArgs), _vp, ctypes.c_size_t, _vp]
+    lib.ssm_scan_fwd_ckpt.restype = ctypes.c_int
+    lib.ssm_scan_bwd_ckpt.argtypes = [ctypes.POINTER(ScanBwdArgs), _vp, ctypes.c_size_t, _vp]
+    lib.ssm_scan_bwd_ckpt.restype = ctypes.c_int
     lib.ssm_conv1d.argtypes = [ctypes.POINTER(Conv1dArgs), _vp]
     lib.ssm_conv1d.restype = ctypes.c_int
     lib.ssm_read_device_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int)]
@@ -275,10 +283,14 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
              h0: Optional[torch.Tensor] = None, return_final_state: bool = True,
              y: Optional[torch.Tensor] = None, h_final: Optional[torch.Tensor] = None,
              workspace: Optional[torch.Tensor] = None, time_chunk: int = 0,
-             stream=None, discretization: str = "euler") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+             stream=None, discretization: str = "euler",
+             checkpoints=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Selective scan.  x, delta, z: (B, L, D); A: (D, N) fp32; B, C: (B, L, N);
     D, delta_bias: (D,) fp32; h0: (B, D, N) fp32; discretization "euler" (B̄ = dl B)
-    or "zoh" (zero-order hold).  Returns (y, h_final)."""
+    or "zoh" (zero-order hold).  Returns (y, h_final).
+    checkpoints: an fp32 tensor of scan_ckpt_shape(...) (or True, to allocate one) that
+    also receives the states scan_bwd rebuilds the sequence from (ssm_scan_fwd_ckpt);
+    the return value is then (y, h_final, checkpoints)."""
     lib = load_library()
     nb, L, Dm = x.shape
     N = A.shape[1]
@@ -293,8 +305,35 @@ def scan_fwd(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Ten
            "ssm_scan_workspace_size")
     ws, nbytes = _workspace(int(need.value), x.device, workspace)
     args.workspace, args.workspace_bytes = _ptr(ws), nbytes
-    _launch(lib.ssm_scan_fwd, args, stream, x.device, "ssm_scan_fwd")
-    return y, h_final
+    if checkpoints is None or checkpoints is False:
+        _launch(lib.ssm_scan_fwd, args, stream, x.device, "ssm_scan_fwd")
+        return y, h_final
+    shape = scan_ckpt_shape(nb, L, Dm, N)
+    if checkpoints is True:
+        checkpoints = torch.empty(shape, dtype=torch.float32, device=x.device)
+    _check(checkpoints, "checkpoints", shape, torch.float32, x.device)
+    fn = lib.ssm_scan_fwd_ckpt
+    with torch.cuda.device(x.device):
+        rc = fn(ctypes.byref(args), _ptr(checkpoints), checkpoints.numel() * 4,
+                _stream(stream, x.device))
+    _raise(rc, "ssm_scan_fwd_ckpt")
+    return y, h_final, checkpoints
+
+
+def scan_ckpt_steps(dstate: int) -> int:
+    """Steps between the state checkpoints the backward pass rebuilds the sequence from."""
+    args = ScanArgs()
+    args.batch, args.seqlen, args.dim, args.dstate = 1, 1, 1, dstate
+    steps, nbytes = ctypes.c_int64(0), ctypes.c_size_t(0)
+    _raise(load_library().ssm_scan_ckpt_size(ctypes.byref(args), ctypes.byref(steps),
+                                             ctypes.byref(nbytes)), "ssm_scan_ckpt_size")
+    return int(steps.value)
+
+
+def scan_ckpt_shape(batch: int, seqlen: int, dim: int, dstate: int) -> Tuple[int, int, int, int]:
+    """(B, ceil(L / T), D, N): the fp32 checkpoint tensor of ssm_scan_fwd_ckpt."""
+    T = scan_ckpt_steps(dstate)
+    return (batch, (seqlen + T - 1) // T, dim, dstate)
 
 
 def scan_bwd(dy: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor,
@@ -302,10 +341,13 @@ def scan_bwd(dy: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torch.Te
              z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
              delta_softplus: bool = True, h0: Optional[torch.Tensor] = None,
              dh_final: Optional[torch.Tensor] = None, discretization: str = "euler",
-             workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+             workspace: Optional[torch.Tensor] = None, stream=None,
+             checkpoints: Optional[torch.Tensor] = None) -> dict:
     """Gradients of scan_fwd with the same inputs, for the gradient dy (B, L, D) of y and
     dh_final (B, D, N) fp32 of the final state (zero when None).  The hidden states
-    are recomputed, not stored.  Returns a dict: dx, ddelta (B, L, D) in x's dtype;
+    are recomputed, not stored: from checkpoints the kernel computes itself, or from
+    `checkpoints` written by scan_fwd(..., checkpoints=...) on the same inputs
+    (ssm_scan_bwd_ckpt).  Returns a dict: dx, ddelta (B, L, D) in x's dtype;
     dz (when z is given); dA (D, N), dB, dC (B, L, N), dD, ddelta_bias (D,), dh0
     (B, D, N), all fp32."""
     lib = load_library()
@@ -328,12 +370,22 @@ def scan_bwd(dy: torch.Tensor, x: torch.Tensor, delta: torch.Tensor, A: torch.Te
                        _ptr(g["ddelta"]), _ptr(g["dz"]), _ptr(g["dA"]), _ptr(g["dB"]),
                        _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
                        None, 0)
-    need = ctypes.c_size_t(0)
-    _raise(lib.ssm_scan_bwd_workspace_size(ctypes.byref(args), ctypes.byref(need)),
-           "ssm_scan_bwd_workspace_size")
-    ws, nbytes = _workspace(int(need.value), dev, workspace)
-    args.workspace, args.workspace_bytes = _ptr(ws), nbytes
-    _launch(lib.ssm_scan_bwd, args, stream, x.device, "ssm_scan_bwd")
+    if checkpoints is not None:
+        _check(checkpoints, "checkpoints", scan_ckpt_shape(nb, L, Dm, N), torch.float32, dev)
+        # the workspace holds only the status word
+        ws, nbytes = _workspace(256, dev, workspace)
+        args.workspace, args.workspace_bytes = _ptr(ws), nbytes
+        with torch.cuda.device(dev):
+            rc = lib.ssm_scan_bwd_ckpt(ctypes.byref(args), _ptr(checkpoints),
+                                       checkpoints.numel() * 4, _stream(stream, dev))
+        _raise(rc, "ssm_scan_bwd_ckpt")
+    else:
+        need = ctypes.c_size_t(0)
+        _raise(lib.ssm_scan_bwd_workspace_size(ctypes.byref(args), ctypes.byref(need)),
+               "ssm_scan_bwd_workspace_size")
+        ws, nbytes = _workspace(int(need.value), dev, workspace)
+        args.workspace, args.workspace_bytes = _ptr(ws), nbytes
+        _launch(lib.ssm_scan_bwd, args, stream, x.device, "ssm_scan_bwd")
     if z is None:
         del g["dz"]
     return g
@@ -546,28 +598,33 @@ def conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] =
 
 # ---------------------------------------------------------------- autograd
 class SelectiveScanFn(torch.autograd.Function):
-    """scan_fwd with its gradients from scan_bwd (hidden states recomputed in the
-    backward pass, nothing but the inputs kept from the forward)."""
+    """scan_fwd with its gradients from scan_bwd.  The hidden states are recomputed in
+    the backward pass from the inputs; with checkpoint_states the forward pass also keeps
+    the state every few steps (scan_fwd(..., checkpoints=True)) and the backward pass
+    starts from those instead of rebuilding them."""
 
     @staticmethod
-    def forward(ctx, x, delta, A, B, C, D, z, delta_bias, h0, delta_softplus, discretization):
-        y, h_final = scan_fwd(x, delta, A, B, C, D=D, z=z, delta_bias=delta_bias,
-                              delta_softplus=delta_softplus, h0=h0,
-                              discretization=discretization)
-        ctx.save_for_backward(x, delta, A, B, C, D, z, delta_bias, h0)
+    def forward(ctx, x, delta, A, B, C, D, z, delta_bias, h0, delta_softplus, discretization,
+                checkpoint_states=False):
+        out = scan_fwd(x, delta, A, B, C, D=D, z=z, delta_bias=delta_bias,
+                       delta_softplus=delta_softplus, h0=h0, discretization=discretization,
+                       checkpoints=True if checkpoint_states else None)
+        y, h_final = out[0], out[1]
+        ck = out[2] if checkpoint_states else None
+        ctx.save_for_backward(x, delta, A, B, C, D, z, delta_bias, h0, ck)
         ctx.delta_softplus, ctx.discretization = delta_softplus, discretization
         return y, h_final
 
     @staticmethod
     def backward(ctx, dy, dh_final):
-        x, delta, A, B, C, D, z, delta_bias, h0 = ctx.saved_tensors
+        x, delta, A, B, C, D, z, delta_bias, h0, ck = ctx.saved_tensors
         need = ctx.needs_input_grad
         if not any(need[:9]):
-            return (None,) * 11
+            return (None,) * 12
         g = scan_bwd(dy.contiguous().to(x.dtype), x, delta, A, B, C, D=D, z=z,
                      delta_bias=delta_bias, delta_softplus=ctx.delta_softplus, h0=h0,
                      dh_final=None if dh_final is None else dh_final.contiguous().float(),
-                     discretization=ctx.discretization)
+                     discretization=ctx.discretization, checkpoints=ck)
 
         def out(i, grad, like):
             # only the inputs autograd asked for get a gradient
@@ -575,16 +632,20 @@ class SelectiveScanFn(torch.autograd.Function):
         return (out(0, g["dx"], x), out(1, g["ddelta"], delta), out(2, g["dA"], A),
                 out(3, g["dB"], B), out(4, g["dC"], C), out(5, g["dD"], D),
                 out(6, g.get("dz"), z), out(7, g["ddelta_bias"], delta_bias),
-                out(8, g["dh0"], h0), None, None)
+                out(8, g["dh0"], h0), None, None, None)
 
 
 def selective_scan(x: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
                    C: torch.Tensor, D: Optional[torch.Tensor] = None,
                    z: Optional[torch.Tensor] = None, delta_bias: Optional[torch.Tensor] = None,
                    h0: Optional[torch.Tensor] = None, delta_softplus: bool = True,
-                   discretization: str = "euler") -> Tuple[torch.Tensor, torch.Tensor]:
+                   discretization: str = "euler",
+                   checkpoint_states: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
     """Differentiable selective scan: (y, h_final) = scan_fwd(...), with every input's
     gradient from the library's backward kernel.  Shapes and dtypes as scan_fwd; the
-    gradients of B and C (fp32 sums over channels) are returned in B's and C's dtype."""
+    gradients of B and C (fp32 sums over channels) are returned in B's and C's dtype.
+    checkpoint_states keeps scan_ckpt_shape(...) fp32 of states from the forward to the
+    backward pass (about D N / T floats per token, T = scan_ckpt_steps(N)) and spares
+    the backward its own forward pass over the sequence."""
     return SelectiveScanFn.apply(x, delta, A, B, C, D, z, delta_bias, h0, delta_softplus,
-                                 discretization)
+                                 discretization, checkpoint_states)

@@ -29,6 +29,10 @@ struct ScanParams {
     uint32_t *flags;
     long long wait_budget;  // clock cycles a block may wait for its predecessors
     int publish;            // 0 only in the look-back self-test: summaries stay unpublished
+    // optional state checkpoints for the backward pass: the state before every step t
+    // with t % 2^ckpt_shift == 0, as (B, ceil(L / 2^ckpt_shift), D, N) fp32; null: none
+    float *ckpt;
+    int ckpt_shift;
 };
 
 // TMA-staged scan (scan_tma.cu): warps per 32-channel block for these sizes (0 = the
@@ -103,8 +107,11 @@ struct ScanBwdParams {
     void *dx, *ddelta, *dz;
     float *dA, *dB, *dC, *dD, *ddelta_bias, *dh0;
     float *ckpt;   // (B, ntiles, D, N) states at the tile starts
+    int ckpt_given;  // 1: ckpt holds them already (written by the forward pass)
 };
 size_t scan_bwd_ckpt_floats(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate);
+// Steps between the backward pass's state checkpoints (its time tile): a power of two.
+int scan_ckpt_steps(int64_t dstate);
 cudaError_t launch_scan_bwd(const ScanBwdParams &p, cudaStream_t stream);
 
 struct Conv1dParams {

@@ -47,6 +47,9 @@ template <int NS> struct BwdShape {
     // steps per tile (and between checkpoints)
     static constexpr int T = NS <= 2 ? 32 : (NS == 4 ? SSM_BWD_TILE_NS4 : 64 / NS);
     static_assert(NS % 2 == 0, "states are processed in packed pairs");
+    // the forward kernels' 32-step tiles hold whole checkpoint intervals, and their 4-step
+    // blocks start at every checkpoint
+    static_assert(T >= 4 && T <= 32 && (T & (T - 1)) == 0, "T must be a power of two in [4, 32]");
     static constexpr int kRows = 9;                              // per-(t, channel) arrays
     static constexpr size_t floats = static_cast<size_t>(T) * kCB * NP   // states
                                      + 2 * T * NP                        // B, C
@@ -261,8 +264,9 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
         const float *h0 = p.h0 + (b * Dm + d) * N + k * NS + 2 * q;
         h[q] = f2{(nval[2 * q] && p.h0) ? h0[0] : 0.f, (nval[2 * q + 1] && p.h0) ? h0[1] : 0.f};
     }
-    if (nt > 1) prefetch(0, T, false);
-    for (int64_t s = 0; s < nt; ++s) {
+    // (skipped when the forward pass wrote the checkpoints)
+    if (nt > 1 && !p.ckpt_given) prefetch(0, T, false);
+    for (int64_t s = 0; s < nt && !p.ckpt_given; ++s) {
         float *ck = p.ckpt + ((b * nt + s) * Dm + d) * N + k * NS;
 #pragma unroll
         for (int q = 0; q < NH; ++q) {
@@ -286,7 +290,8 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
             }
         }
     }
-    // the checkpoint stores of this block are read back by the same threads below
+    // the checkpoint stores of this block are read back by the same threads below; the
+    // forward pass's are visible to this launch
 
     // ---- 2. reverse pass
     f2 lam[NH], gA[NH];
@@ -508,17 +513,17 @@ cudaError_t launch_typed(const ScanBwdParams &p, cudaStream_t stream) {
     return launch_ns<TIO, 16, kZoh>(p, stream);
 }
 
-int tile_steps(int64_t dstate) {
+}  // namespace
+
+int scan_ckpt_steps(int64_t dstate) {
     if (dstate <= 8) return BwdShape<2>::T;
     if (dstate <= 16) return BwdShape<4>::T;
     if (dstate <= 32) return BwdShape<8>::T;
     return BwdShape<16>::T;
 }
 
-}  // namespace
-
 size_t scan_bwd_ckpt_floats(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate) {
-    const int64_t T = tile_steps(dstate);
+    const int64_t T = scan_ckpt_steps(dstate);
     const int64_t nt = (seqlen + T - 1) / T;
     return static_cast<size_t>(batch * nt * dim * dstate);
 }

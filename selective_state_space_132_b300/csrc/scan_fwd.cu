@@ -60,7 +60,7 @@ template <int NS, int LPC, bool kSummary> struct ScanSmem {
     static constexpr size_t bytes = sizeof(float) * total;
 };
 
-template <typename TIO, int NS, int LPC, bool kSummary, bool kFast>
+template <typename TIO, int NS, int LPC, bool kSummary, bool kFast, bool kCkpt>
 __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(ScanParams p) {
     constexpr int NT = kDT * LPC;
     constexpr int NP = NS * LPC;
@@ -134,6 +134,9 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
         }
     }
     float dsum_acc = 0.f;
+    // checkpoints along the whole sequence (the backward pass's time tiles)
+    const int64_t ck_tiles = kCkpt ? (L + (int64_t(1) << p.ckpt_shift) - 1) >> p.ckpt_shift : 0;
+    (void)ck_tiles;
 
     // raw-input prefetch registers for one tile
     TIO rx[kQuadIters * 4], rdl[kQuadIters * 4], rz[kQuadIters * 4];
@@ -225,6 +228,17 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
             float yq[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
+                if constexpr (kCkpt && !kSummary) {
+                    // the state before step t0 + tq, at every checkpoint step (at least
+                    // four steps apart, so only i = 0 can have one)
+                    const int64_t t = t0 + tq + i;
+                    if (i == 0 && (tq & ((1 << p.ckpt_shift) - 1)) == 0 && dval && t < t_end) {
+                        float *ck = p.ckpt + ((b * ck_tiles + (t >> p.ckpt_shift)) * D + d) * N;
+#pragma unroll
+                        for (int k = 0; k < NS; ++k)
+                            if (j * NS + k < N) ck[j * NS + k] = h[k];
+                    }
+                }
                 float bv[NS], cv[NS];
 #pragma unroll
                 for (int k4 = 0; k4 < NS; k4 += 4) {
@@ -308,10 +322,10 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
     }
 }
 
-template <typename TIO, int NS, int LPC, bool kSummary>
+template <typename TIO, int NS, int LPC, bool kSummary, bool kCkpt = false>
 cudaError_t launch_one(const ScanParams &p, int nchunks_grid, cudaStream_t stream) {
     constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
-    auto kern = scan_kernel<TIO, NS, LPC, kSummary, kFast>;
+    auto kern = scan_kernel<TIO, NS, LPC, kSummary, kFast, kCkpt>;
     const size_t smem = ScanSmem<NS, LPC, kSummary>::bytes;
     if (smem > 48 * 1024) {
         cudaError_t e =
@@ -330,7 +344,9 @@ cudaError_t launch_pair(const ScanParams &p, cudaStream_t stream) {
         cudaError_t e = launch_one<TIO, NS, LPC, true>(p, p.nchunks - 1, stream);
         if (e != cudaSuccess) return e;
     }
-    return launch_one<TIO, NS, LPC, false>(p, p.nchunks, stream);
+    // the output pass writes the backward pass's state checkpoints when asked to
+    return p.ckpt ? launch_one<TIO, NS, LPC, false, true>(p, p.nchunks, stream)
+                  : launch_one<TIO, NS, LPC, false, false>(p, p.nchunks, stream);
 }
 
 template <typename TIO> cudaError_t launch_typed(const ScanParams &p, cudaStream_t stream) {

@@ -59,6 +59,8 @@ constexpr int kStages = SSM_SCAN_STAGES;  // TMA pipeline depth
 #define SSM_SCAN_UNROLL 4
 #endif
 constexpr int kU = SSM_SCAN_UNROLL;  // time steps per ILP block of the scan loop
+// state checkpoints (every 4 to 32 steps) fall on the first step of an ILP block
+static_assert(kU <= 4 && kT % kU == 0, "checkpoint steps must be multiples of kU");
 #ifndef SSM_SCAN_LOOKBACK
 #define SSM_SCAN_LOOKBACK 1
 #endif
@@ -172,7 +174,7 @@ template <bool kFast> __device__ __forceinline__ f2 decay2(float dl, f2 a) {
 // store) and the summary pass publishes its own.  Returns false after a bounded wait
 // gave up (the status word then says so).
 template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kLB,
-          bool kRed>
+          bool kRed, bool kCkpt>
 __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams &p, int b,
                                            int c, int d0, int slab) {
     using LY = Layout<TIO, NS, LPC, WPC, kSummary, kRed>;
@@ -304,6 +306,9 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
     }
     float dsum = 0.f;
     int failed_tile = -1;
+    // checkpoints along the whole sequence (the backward pass's time tiles)
+    const int64_t ck_tiles = kCkpt ? (L + (int64_t(1) << p.ckpt_shift) - 1) >> p.ckpt_shift : 0;
+    (void)ck_tiles;
 
     for (int tile = 0; tile < ntiles; ++tile) {
         const int s = tile % kStages;
@@ -422,6 +427,17 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
                         } else {
                             uv[u][k] = ptx::mul2(f2{dx[u], dx[u]}, bp[u][k]);
                         }
+                    }
+                }
+                if constexpr (kCkpt && !kSummary) {
+                    // the state before step t0 + tb, at every checkpoint step (checkpoints
+                    // are at least kU steps apart, so only a block's first step has one)
+                    const int64_t t = t0 + tb;
+                    if ((tb & ((1 << p.ckpt_shift) - 1)) == 0 && sdval && t < t_end) {
+                        float2 *ck = reinterpret_cast<float2 *>(
+                            p.ckpt + ((b * ck_tiles + (t >> p.ckpt_shift)) * D + sd) * N + j * NS);
+#pragma unroll
+                        for (int k = 0; k < NS / 2; ++k) ck[k] = make_float2(h[k].x, h[k].y);
                     }
                 }
                 float acc[kU];
@@ -545,7 +561,8 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
 }
 
 // Two-launch form: the summary pass over chunks 0 .. K-2, then the output pass.
-template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kRed>
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kRed,
+          bool kCkpt>
 __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constant__ TmaMaps maps,
                                                             ScanParams p) {
     using LY = Layout<TIO, NS, LPC, WPC, kSummary, kRed>;
@@ -554,7 +571,7 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
     if (p.clear_status && status && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
         blockIdx.z == 0)
         status->code = 0;
-    (void)chunk_pass<TIO, NS, LPC, WPC, kSummary, kZoh, false, kRed>(
+    (void)chunk_pass<TIO, NS, LPC, WPC, kSummary, kZoh, false, kRed, kCkpt>(
         maps, p, blockIdx.y, blockIdx.z, blockIdx.x * LY::CPB, blockIdx.x);
 }
 
@@ -567,7 +584,7 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
 // they are bounded all the same.  Every chunk but the last is still read twice (summary
 // and output), as in the two-launch form; what goes is the launch boundary between the
 // passes and the idle tail of the first launch.
-template <typename TIO, int NS, int LPC, int WPC, bool kZoh, bool kRed>
+template <typename TIO, int NS, int LPC, int WPC, bool kZoh, bool kRed, bool kCkpt>
 __global__ void __launch_bounds__(32 * WPC) scan_tma_lb_kernel(const __grid_constant__ TmaMaps maps,
                                                                ScanParams p) {
     using LY = Layout<TIO, NS, LPC, WPC, false, kRed>;
@@ -580,18 +597,20 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_lb_kernel(const __grid_cons
     const int c = ticket / per_chunk, r = ticket % per_chunk;
     const int b = r / nslabs, slab = r % nslabs;
     if (c < p.nchunks - 1 &&
-        !chunk_pass<TIO, NS, LPC, WPC, true, kZoh, true, kRed>(maps, p, b, c, slab * LY::CPB, slab))
+        !chunk_pass<TIO, NS, LPC, WPC, true, kZoh, true, kRed, false>(maps, p, b, c,
+                                                                      slab * LY::CPB, slab))
         return;
-    (void)chunk_pass<TIO, NS, LPC, WPC, false, kZoh, true, kRed>(maps, p, b, c, slab * LY::CPB,
-                                                                   slab);
+    (void)chunk_pass<TIO, NS, LPC, WPC, false, kZoh, true, kRed, kCkpt>(maps, p, b, c,
+                                                                          slab * LY::CPB, slab);
 }
 
 // ---------------------------------------------------------------- host side
-template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kRed>
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kRed,
+          bool kCkpt>
 cudaError_t launch_tma_one(const ScanParams &p, const TmaMaps &maps, int nchunks_grid,
                            cudaStream_t stream) {
     using LY = Layout<TIO, NS, LPC, WPC, kSummary, kRed>;
-    auto kern = scan_tma_kernel<TIO, NS, LPC, WPC, kSummary, kZoh, kRed>;
+    auto kern = scan_tma_kernel<TIO, NS, LPC, WPC, kSummary, kZoh, kRed, kCkpt>;
     if (LY::bytes > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              LY::bytes);
@@ -604,7 +623,7 @@ cudaError_t launch_tma_one(const ScanParams &p, const TmaMaps &maps, int nchunks
 }
 
 // Blocks of 32 channels: WPC = LPC warps of 32 / LPC channels each.
-template <typename TIO, int NS, int LPC, bool kZoh>
+template <typename TIO, int NS, int LPC, bool kZoh, bool kCkpt>
 cudaError_t launch_tma_pair(ScanParams p, cudaStream_t stream) {
     constexpr int WPC = LPC;
     using LY = Layout<TIO, NS, LPC, WPC, false>;
@@ -623,7 +642,7 @@ cudaError_t launch_tma_pair(ScanParams p, cudaStream_t stream) {
         // one launch, the chunk summaries handed over through the look-back flags (the
         // caller zeroed the status word, the ticket and the flags)
         using LR = Layout<TIO, NS, LPC, WPC, false, kSplitRed>;
-        auto kern = scan_tma_lb_kernel<TIO, NS, LPC, WPC, kZoh, kSplitRed>;
+        auto kern = scan_tma_lb_kernel<TIO, NS, LPC, WPC, kZoh, kSplitRed, kCkpt>;
         if (LR::bytes > 48 * 1024) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  LR::bytes);
@@ -634,13 +653,21 @@ cudaError_t launch_tma_pair(ScanParams p, cudaStream_t stream) {
         return cudaGetLastError();
     }
     if (p.nchunks > 1) {
-        cudaError_t e =
-            launch_tma_one<TIO, NS, LPC, WPC, true, kZoh, false>(p, m, p.nchunks - 1, stream);
+        cudaError_t e = launch_tma_one<TIO, NS, LPC, WPC, true, kZoh, false, false>(
+            p, m, p.nchunks - 1, stream);
         if (e != cudaSuccess) return e;
         p.clear_status = 0;
-        return launch_tma_one<TIO, NS, LPC, WPC, false, kZoh, kSplitRed>(p, m, p.nchunks, stream);
+        return launch_tma_one<TIO, NS, LPC, WPC, false, kZoh, kSplitRed, kCkpt>(p, m, p.nchunks,
+                                                                                stream);
     }
-    return launch_tma_one<TIO, NS, LPC, WPC, false, kZoh, false>(p, m, p.nchunks, stream);
+    return launch_tma_one<TIO, NS, LPC, WPC, false, kZoh, false, kCkpt>(p, m, p.nchunks, stream);
+}
+
+// with or without state checkpoints for the backward pass
+template <typename TIO, int NS, int LPC, bool kZoh>
+cudaError_t launch_tma_ck(const ScanParams &p, cudaStream_t stream) {
+    return p.ckpt ? launch_tma_pair<TIO, NS, LPC, kZoh, true>(p, stream)
+                  : launch_tma_pair<TIO, NS, LPC, kZoh, false>(p, stream);
 }
 
 }  // namespace
@@ -707,17 +734,17 @@ template <bool kZoh> cudaError_t launch_scan_tma_disc(const ScanParams &p, cudaS
     const int64_t N = p.dstate;
     if (p.io_bf16) {
         using T = __nv_bfloat16;
-        if (N == 8) return launch_tma_pair<T, 4, 2, kZoh>(p, stream);
-        if (N == 16) return launch_tma_pair<T, 4, 4, kZoh>(p, stream);
-        if (N == 32) return launch_tma_pair<T, 8, 4, kZoh>(p, stream);
-        if (N == 64) return launch_tma_pair<T, 16, 4, kZoh>(p, stream);
+        if (N == 8) return launch_tma_ck<T, 4, 2, kZoh>(p, stream);
+        if (N == 16) return launch_tma_ck<T, 4, 4, kZoh>(p, stream);
+        if (N == 32) return launch_tma_ck<T, 8, 4, kZoh>(p, stream);
+        if (N == 64) return launch_tma_ck<T, 16, 4, kZoh>(p, stream);
     } else {
         using T = float;
-        if (N == 4) return launch_tma_pair<T, 2, 2, kZoh>(p, stream);
-        if (N == 8) return launch_tma_pair<T, 4, 2, kZoh>(p, stream);
-        if (N == 16) return launch_tma_pair<T, 4, 4, kZoh>(p, stream);
-        if (N == 32) return launch_tma_pair<T, 8, 4, kZoh>(p, stream);
-        if (N == 64) return launch_tma_pair<T, 16, 4, kZoh>(p, stream);
+        if (N == 4) return launch_tma_ck<T, 2, 2, kZoh>(p, stream);
+        if (N == 8) return launch_tma_ck<T, 4, 2, kZoh>(p, stream);
+        if (N == 16) return launch_tma_ck<T, 4, 4, kZoh>(p, stream);
+        if (N == 32) return launch_tma_ck<T, 8, 4, kZoh>(p, stream);
+        if (N == 64) return launch_tma_ck<T, 16, 4, kZoh>(p, stream);
     }
     return cudaErrorInvalidValue;
 }

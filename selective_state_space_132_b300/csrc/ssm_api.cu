@@ -340,10 +340,19 @@ ssm_status ssm_scan_plan(const ssm_scan_args *a, int64_t *chunk_len, int32_t *nc
 }  // extern "C"
 
 namespace {
+int ckpt_shift(int64_t dstate) {
+    int sh = 0;
+    while ((1 << sh) < ssm::scan_ckpt_steps(dstate)) ++sh;
+    return sh;
+}
+// Bytes of the state checkpoints of these sizes: (B, ceil(L / T), D, N) fp32.
+size_t ckpt_bytes_for(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate) {
+    return ssm::scan_bwd_ckpt_floats(batch, seqlen, dim, dstate) * sizeof(float);
+}
 // The scan call; `budget` and `publish` differ from the defaults only in the look-back
-// self-test.
+// self-test; `ckpt` (nullable) receives the backward pass's state checkpoints.
 ssm_status scan_fwd_impl(const ssm_scan_args *a, ssm_stream_t stream, long long budget,
-                         int publish) {
+                         int publish, float *ckpt = nullptr) {
     ssm_status s = check_scan(a);
     if (s != SSM_OK) return s;
     int64_t cl;
@@ -376,6 +385,8 @@ ssm_status scan_fwd_impl(const ssm_scan_args *a, ssm_stream_t stream, long long 
     p.zoh = a->discretization == SSM_DISC_ZOH;
     p.wait_budget = budget;
     p.publish = publish;
+    p.ckpt = ckpt;
+    p.ckpt_shift = ckpt_shift(a->dstate);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the status word starts at zero
     if (cudaMemsetAsync(a->workspace, 0, kStatusBytes, st) != cudaSuccess) return SSM_ERR_CUDA;
@@ -401,6 +412,40 @@ extern "C" {
 ssm_status ssm_scan_fwd(const ssm_scan_args *a, ssm_stream_t stream) {
     NvtxRange nvtx("ssm_scan_fwd");
     return scan_fwd_impl(a, stream, ssm::kScanWaitCycles, 1);
+}
+
+ssm_status ssm_scan_ckpt_size(const ssm_scan_args *a, int64_t *steps, size_t *bytes) {
+    if (!steps || !bytes) return SSM_ERR_INVALID_ARG;
+    ssm_status s = check_scan(a, false);
+    if (s != SSM_OK) return s;
+    *steps = ssm::scan_ckpt_steps(a->dstate);
+    *bytes = ckpt_bytes_for(a->batch, a->seqlen, a->dim, a->dstate);
+    return SSM_OK;
+}
+
+ssm_status ssm_scan_fwd_ckpt(const ssm_scan_args *a, float *ckpt, size_t ckpt_bytes,
+                             ssm_stream_t stream) {
+    NvtxRange nvtx("ssm_scan_fwd_ckpt");
+    ssm_status s = check_scan(a);
+    if (s != SSM_OK) return s;
+    const size_t need = ckpt_bytes_for(a->batch, a->seqlen, a->dim, a->dstate);
+    if (need > 0 && !ckpt) return SSM_ERR_INVALID_ARG;
+    if (ckpt_bytes < need) return SSM_ERR_INVALID_ARG;
+    if (ckpt && !aligned(ckpt, 16)) return SSM_ERR_ALIGNMENT;
+    // the checkpoints are an output: they may overlap no input and no other output
+    const size_t e = io_size(a->io_dtype);
+    const size_t tok = (size_t)(a->batch * a->seqlen * a->dim) * e;
+    const size_t bc = (size_t)(a->batch * a->seqlen * a->dstate) * e;
+    const size_t st = (size_t)(a->batch * a->dim * a->dstate) * 4;
+    const void *toks[] = {a->x, a->delta, a->z, a->y};
+    for (const void *q : toks)
+        if (overlaps(ckpt, need, q, tok)) return SSM_ERR_INVALID_ARG;
+    if (overlaps(ckpt, need, a->B, bc) || overlaps(ckpt, need, a->C, bc) ||
+        overlaps(ckpt, need, a->h0, st) || overlaps(ckpt, need, a->h_final, st) ||
+        overlaps(ckpt, need, a->A, (size_t)(a->dim * a->dstate) * 4) ||
+        overlaps(ckpt, need, a->workspace, a->workspace_bytes))
+        return SSM_ERR_INVALID_ARG;
+    return scan_fwd_impl(a, stream, ssm::kScanWaitCycles, 1, need > 0 ? ckpt : nullptr);
 }
 
 ssm_status ssm_check_scan_lookback(const ssm_scan_args *a, int64_t budget_cycles,
@@ -510,10 +555,20 @@ ssm_status ssm_scan_bwd_workspace_size(const ssm_scan_bwd_args *a, size_t *bytes
     return SSM_OK;
 }
 
-ssm_status ssm_scan_bwd(const ssm_scan_bwd_args *a, ssm_stream_t stream) {
-    NvtxRange nvtx("ssm_scan_bwd");
+}  // extern "C"
+
+namespace {
+// The backward call; `ckpt` (nullable) holds the state checkpoints a forward pass wrote,
+// otherwise the kernel computes them in the workspace.
+ssm_status scan_bwd_impl(const ssm_scan_bwd_args *a, ssm_stream_t stream, const float *ckpt,
+                         size_t ckpt_bytes) {
     ssm_status s = check_scan_bwd(a);
     if (s != SSM_OK) return s;
+    if (ckpt) {
+        if (ckpt_bytes < ckpt_bytes_for(a->batch, a->seqlen, a->dim, a->dstate))
+            return SSM_ERR_INVALID_ARG;
+        if (!aligned(ckpt, 16)) return SSM_ERR_ALIGNMENT;
+    }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int64_t rows = a->batch * a->seqlen;
     // the sums start at zero; with no channels or no rows only they are written
@@ -544,7 +599,8 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_args *a, ssm_stream_t stream) {
         }
         return SSM_OK;
     }
-    const size_t need = scan_bwd_ws(a);
+    // with given checkpoints the workspace holds only the status word
+    const size_t need = ckpt ? ssm::kStatusBytes : scan_bwd_ws(a);
     if (!a->workspace || a->workspace_bytes < need) return SSM_ERR_WORKSPACE;
     if (!aligned(a->workspace, 256)) return SSM_ERR_ALIGNMENT;
     ssm::ScanBwdParams p{};
@@ -575,8 +631,25 @@ ssm_status ssm_scan_bwd(const ssm_scan_bwd_args *a, ssm_stream_t stream) {
     p.dD = a->dD;
     p.ddelta_bias = a->ddelta_bias;
     p.dh0 = a->dh0;
-    p.ckpt = reinterpret_cast<float *>(static_cast<char *>(a->workspace) + ssm::kStatusBytes);
+    p.ckpt = ckpt ? const_cast<float *>(ckpt)
+                  : reinterpret_cast<float *>(static_cast<char *>(a->workspace) + ssm::kStatusBytes);
+    p.ckpt_given = ckpt ? 1 : 0;
     return from_cuda(ssm::launch_scan_bwd(p, st));
+}
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_scan_bwd(const ssm_scan_bwd_args *a, ssm_stream_t stream) {
+    NvtxRange nvtx("ssm_scan_bwd");
+    return scan_bwd_impl(a, stream, nullptr, 0);
+}
+
+ssm_status ssm_scan_bwd_ckpt(const ssm_scan_bwd_args *a, const float *ckpt, size_t ckpt_bytes,
+                             ssm_stream_t stream) {
+    NvtxRange nvtx("ssm_scan_bwd_ckpt");
+    if (!ckpt) return SSM_ERR_INVALID_ARG;
+    return scan_bwd_impl(a, stream, ckpt, ckpt_bytes);
 }
 
 ssm_status ssm_conv1d(const ssm_conv1d_args *a, ssm_stream_t stream) {
