@@ -29,9 +29,14 @@ def test_bench_prints_contract_line():
     c = d["config"]
     per_call = ssm.scan_launches_per_call(c["batch"], c["seqlen"], c["d_inner"], c["d_state"])
     assert d["gpu_launches"] == 5 * per_call
+    # the scan is dispatch-bound: the ALU roofline, with the HBM one beside it
     r = d["roofline"]
-    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and 0 < r["frac"] < 1.5
+    assert r["bound"] == "alu" and r["unit"] == "state-updates/s" and 0 < r["frac"] < 1.5
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    assert abs(r["achieved"] - d["value"]) <= 0.05 * d["value"]
+    h = r["hbm"]
+    assert h["bound"] == "hbm" and h["unit"] == "GB/s" and 0 < h["frac"] < 1.5
+    assert abs(h["frac"] - h["achieved"] / h["peak"]) < 1e-9
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert "workload" in d["config"] and "l2" in d["config"]
