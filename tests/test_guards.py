@@ -152,3 +152,34 @@ def test_scan_bwd_writes_stay_inside_and_repeat(io, D, N):
         assert torch.equal(g[k].t, first[k]), k
     for k in ("dA", "dB", "dC", "dD", "ddelta_bias"):  # summed with fp32 atomics
         assert torch.allclose(g[k].t, first[k], rtol=1e-5, atol=1e-6), k
+
+
+@pytest.mark.parametrize("io,D,N,tc", [("bf16", 64, 16, 0), ("bf16", 64, 16, 32),
+                                       ("f32", 45, 5, 0), ("bf16", 32, 64, 0)])
+def test_scan_checkpoints_stay_inside_and_repeat(io, D, N, tc):
+    """ssm_scan_fwd_ckpt writes the checkpoints inside their buffer (ragged last
+    checkpoint interval: L = 77), the same on every call, and ssm_scan_bwd_ckpt reads
+    them without writing outside its outputs."""
+    p, a = _scan_inputs(io, D, N)
+    t = io_dtype(io)
+    shape = ssm.scan_ckpt_shape(p.batch, p.seqlen, D, N)
+    ck = Guarded(shape, torch.float32)
+    y = Guarded((p.batch, p.seqlen, D), t)
+
+    def fwd():
+        ssm.scan_fwd(a["x"], a["delta"], a["A"], a["B"], a["C"], D=a["D"], z=a["z"],
+                     delta_bias=a["delta_bias"], h0=a["h0"], y=y.t, time_chunk=tc,
+                     checkpoints=ck.t)
+        torch.cuda.synchronize()
+    fwd()
+    assert ck.intact() and y.intact()
+    first = ck.t.clone()
+    fwd()
+    assert torch.equal(ck.t, first)
+    dy = dev(np.random.default_rng(4).standard_normal((p.batch, p.seqlen, D)), t)
+    dx = Guarded((p.batch, p.seqlen, D), t)
+    g = ssm.scan_bwd(dy, a["x"], a["delta"], a["A"], a["B"], a["C"], D=a["D"], z=a["z"],
+                     delta_bias=a["delta_bias"], h0=a["h0"], checkpoints=ck.t)
+    dx.t.copy_(g["dx"])
+    torch.cuda.synchronize()
+    assert ck.intact() and torch.equal(ck.t, first)
