@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
         commit(false);
         if (s + 2 < nt) prefetch((s + 1) * T, T, false);
         __syncthreads();
-#pragma unroll 2
+#pragma unroll 8
         for (int t = 0; t < T; ++t) {
             const float dl = sdl[t * kCB + c], xv = sx[t * kCB + c];
             f2 Bp[NH];
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
         // recompute h_t of the tile (and C.h + D x for the gate's gradient)
 #pragma unroll
         for (int q = 0; q < NH; ++q) h[q] = hst[q];
-#pragma unroll 2
+#pragma unroll 8
         for (int t = 0; t < Ts; ++t) {
             const float dl = sdl[t * kCB + c], xv = sx[t * kCB + c];
             f2 Bp[NH], Cp[NH];
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
             if (k == 0) syr[t * kCB + c] = fmaf(Dd, xv, part);
         }
         // walk the tile backwards; h holds h_t, hp is h_{t-1}
-#pragma unroll 2
+#pragma unroll 8
         for (int t = Ts - 1; t >= 0; --t) {
             f2 hp[NH];
             if (t > 0) {
