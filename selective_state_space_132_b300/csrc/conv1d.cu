@@ -212,18 +212,22 @@ __global__ void __launch_bounds__(kBlockT) conv1d_tma_kernel(const __grid_consta
     const int tid = threadIdx.x;
     const int q = tid % CH, rg = tid / CH;
     const int64_t D = p.dim, L = p.seqlen;
-    const int64_t nds = (D + TD - 1) / TD, nts = (L + kTT - 1) / kTT;
-    const int64_t nstrips = p.batch * nts;
-    const int64_t ntiles = nds * nstrips;
+    // tile indices fit in 32 bits (the host checks the tile count), so the per-tile
+    // coordinates take 32-bit divisions
+    const uint32_t nds = static_cast<uint32_t>((D + TD - 1) / TD);
+    const uint32_t nts = static_cast<uint32_t>((L + kTT - 1) / kTT);
+    const uint32_t nstrips = static_cast<uint32_t>(p.batch) * nts;
+    const uint32_t ntiles = nds * nstrips;
     // this block's contiguous range [k0, k1) of tiles
-    const int64_t G = gridDim.x, per = ntiles / G, rem = ntiles % G;
-    const int64_t k0 = blockIdx.x * per + (blockIdx.x < rem ? blockIdx.x : rem);
-    const int64_t k1 = k0 + per + (blockIdx.x < rem ? 1 : 0);
-    auto coords = [&](int64_t k, int &d0, int &t0, int &b) {
-        d0 = static_cast<int>((k / nstrips) * TD);
-        const int64_t strip = k % nstrips;
-        b = static_cast<int>(strip / nts);
-        t0 = static_cast<int>((strip % nts) * kTT);
+    const uint32_t G = gridDim.x, per = ntiles / G, rem = ntiles % G;
+    const uint32_t k0 = blockIdx.x * per + (blockIdx.x < rem ? blockIdx.x : rem);
+    const uint32_t k1 = k0 + per + (blockIdx.x < rem ? 1 : 0);
+    auto coords = [&](uint32_t k, int &d0, int &t0, int &b) {
+        const uint32_t slab = k / nstrips, strip = k - slab * nstrips;
+        const uint32_t bb = strip / nts;
+        d0 = static_cast<int>(slab * TD);
+        b = static_cast<int>(bb);
+        t0 = static_cast<int>((strip - bb * nts) * kTT);
     };
 
     if (tid == 0) {
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kBlockT) conv1d_tma_kernel(const __grid_consta
     int cur_d0 = -1;
     bool cin = false;
     int64_t failed = -1;
-    for (int64_t k = k0; k < k1; ++k) {
+    for (uint32_t k = k0; k < k1; ++k) {
         const int it = static_cast<int>(k - k0);
         const int s = it % kStagesT;
         // the y buffer of this tile was last stored two tiles ago
@@ -420,9 +424,14 @@ int conv1d_max_width() { return kMaxK; }
 bool conv1d_tma_ok(const Conv1dParams &p) {
     const size_t e = p.io_bf16 ? 2 : 4;
     auto a16 = [](const void *q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+    if (p.seqlen >= (int64_t(1) << 31) || p.batch >= (int64_t(1) << 31) ||
+        p.dim >= (int64_t(1) << 31))
+        return false;
+    // the kernel indexes its tiles in 32 bits
+    const int64_t tiles = p.batch * ((p.seqlen + kTT - 1) / kTT) *
+                          ((p.dim * static_cast<int64_t>(e) + kRowB - 1) / kRowB);
     return (p.dim * e) % 16 == 0 && a16(p.x) && a16(p.out) && a16(p.x_prev) && a16(p.weight) &&
-           a16(p.bias) && p.seqlen < (int64_t(1) << 31) &&
-           p.batch < (int64_t(1) << 31) && p.dim < (int64_t(1) << 31) && tma_encoder() != nullptr;
+           a16(p.bias) && tiles < (int64_t(1) << 31) && tma_encoder() != nullptr;
 }
 
 cudaError_t launch_conv1d(const Conv1dParams &p, cudaStream_t stream) {
