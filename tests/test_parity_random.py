@@ -59,10 +59,19 @@ def test_random_scan_bwd(case):
     t = io_dtype(io)
     gy = rng.standard_normal((nb, L, D)).astype(np.float32)
     ghf = rng.standard_normal((nb, D, N)).astype(np.float32) if case % 3 else None
+    disc = "zoh" if zoh else "euler"
+    ck = None
+    if case % 4 >= 2:
+        # half of the cases start the backward from the forward pass's checkpoints (the
+        # forward whole or split over time chunks)
+        ck = ssm.scan_fwd(dev(p.x, t), dev(p.delta, t), dev(p.A), dev(p.B, t), dev(p.C, t),
+                          D=dev(p.D), z=dev(p.z, t), delta_bias=dev(p.bias),
+                          delta_softplus=sp, h0=dev(p.h0), discretization=disc,
+                          time_chunk=int(rng.choice([0, 32, 64])), checkpoints=True)[2]
     g = ssm.scan_bwd(dev(gy, t), dev(p.x, t), dev(p.delta, t), dev(p.A), dev(p.B, t),
                      dev(p.C, t), D=dev(p.D), z=dev(p.z, t), delta_bias=dev(p.bias),
                      delta_softplus=sp, h0=dev(p.h0), dh_final=dev(ghf),
-                     discretization="zoh" if zoh else "euler")
+                     discretization=disc, checkpoints=ck)
     torch.cuda.synchronize()
     rnd = lambda a: None if a is None else host(dev(a, t))          # noqa: E731
     ref = oracle.scan_bwd(rnd(gy), rnd(p.x), rnd(p.delta), p.A, rnd(p.B), rnd(p.C), Dv=p.D,
