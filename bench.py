@@ -46,10 +46,10 @@ L2_FLUSH_BYTES = 256 << 20
 # kernel's sources at the time of the capture and by workload; an entry whose key no
 # longer matches the sources is ignored (traffic reported as null).
 PROFILED_TRAFFIC = {
-    "3079d47a07ffe413": {
+    "0e48fe664cffe602": {
         # scan_tma_lb_kernel (summary and output passes in one launch), mean of 5 calls:
-        # 3,221.6 MB read + 525.7 MB written (profiles/scan_tma_bf16_B1_D2048_L131072_N16.md)
-        "scan_bf16_B1_D2048_L131072_N16": 3747300000,
+        # 3,046.2 MB read + 528.9 MB written (profiles/scan_tma_bf16_B1_D2048_L131072_N16.md)
+        "scan_bf16_B1_D2048_L131072_N16": 3575100000,
     },
 }
 
@@ -728,11 +728,17 @@ def run_ours(args, world, rank, local):
         if world == 1 and not args.no_cpu:
             out["cpu_baseline"] = cpu_baseline_scan(p)
         if not args.no_extras and world == 1:
-            out["kernels"] = extras(device, flush, hbm, tf_sus, skip=(args.workload,))
+            ks = ClockSampler(local)
+            ks.start()
+            try:
+                out["kernels"] = extras(device, flush, hbm, tf_sus, skip=(args.workload,),
+                                        sampler=ks)
+            finally:
+                ks.stop()
     return out
 
 
-def extras(device, flush, hbm, tf_sus, only=None, iters=None, skip=()):
+def extras(device, flush, hbm, tf_sus, only=None, iters=None, skip=(), sampler=None):
     """The other workloads, one measurement each (parity cases, not the bench line).
     `only` runs one of them alone and `iters` sets its timed iterations (both used to
     profile one kernel with ncu)."""
@@ -857,7 +863,11 @@ def extras(device, flush, hbm, tf_sus, only=None, iters=None, skip=()):
     for name, fn in runners.items():
         if (only is not None and name != only) or name in skip:
             continue
+        t0 = time.time()
         res[name] = fn()
+        if sampler is not None:
+            # the SM clocks and throttle reasons while this workload ran
+            res[name]["clocks"] = sampler.summary(t0, time.time())
         torch.cuda.empty_cache()
     return res
 
