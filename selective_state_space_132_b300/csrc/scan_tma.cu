@@ -112,7 +112,10 @@ template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kRed = fal
     static constexpr int o_part = o_dlx + align1k(CPB * kDlxRow * 4);
     static constexpr int o_y = o_part + (kSummary ? 0 : align1k(WPC * kSlots * kPart * 4));
     static constexpr int o_bar = o_y + (kSummary ? 0 : 2 * align1k(kTok));
-    static constexpr int bytes = o_bar + kStages * 8 + 1024;  // + slack to align the base
+    // summary pass with bf16 I/O: B widened to fp32 once per tile by the block
+    static constexpr int o_bf32 = align1k(o_bar + kStages * 8);
+    static constexpr int bytes = (kSummary && E == 2 ? o_bf32 + kT * N * 4 : o_bar + kStages * 8) +
+                                 1024;  // + slack to align the base
 };
 
 struct TmaMaps {
@@ -317,9 +320,20 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
         const bool got = ptx::mbar_wait(&bars[s], (tile / kStages) & 1);
 
         // ---------------- prologue (only after this thread's own wait succeeded)
-        const float *Bf = reinterpret_cast<const float *>(st + LY::s_B);   // fp32 I/O
+        constexpr bool kWidenB = kSummary && LY::kRawBC;
+        const float *Bf = kWidenB ? reinterpret_cast<const float *>(smem + LY::o_bf32)
+                                  : reinterpret_cast<const float *>(st + LY::s_B);   // fp32 I/O
         const float *Cf = reinterpret_cast<const float *>(st + LY::s_C);
         if (got) {
+            if constexpr (kWidenB) {
+                // the block widens the tile's B (kT x N bf16) once for all its lanes
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(st + LY::s_B);
+                float2 *dst = reinterpret_cast<float2 *>(smem + LY::o_bf32);
+                for (int e = tid; e < kT * N / 2; e += 32 * WPC) {
+                    const ptx::f2 v = ptx::bf2_to_f2(src[e]);
+                    dst[e] = make_float2(v.x, v.y);
+                }
+            }
             const bool tval = t0 + lane < t_end;
 #pragma unroll
             for (int q = 0; q < QW; ++q) {
@@ -359,7 +373,7 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
                 f2 bp[kU][NS / 2], cp[kU][NS / 2];
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
-                    if constexpr (LY::kRawBC) {
+                    if constexpr (LY::kRawBC && !kWidenB) {
                         // NS bf16 values = NS / 2 words per row, 8- or 16-byte loads
                         const uint32_t *Bw = reinterpret_cast<const uint32_t *>(st + LY::s_B) +
                                              ((tb + u) * N + j * NS) / 2;
@@ -462,15 +476,25 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
                         part[j * LY::kPart + (tb + u) * LY::kPartT + sc] = acc[u];
                 }
                 if (!kSummary && kRed) {
-                    // sum over the channel's LPC adjacent lanes; lane slot j then stores
-                    // the steps u with u % LPC == j
+                    // sum over the channel's LPC adjacent lanes as a reduce-scatter: at
+                    // lane bit m every lane keeps the steps whose bit m matches its own
+                    // and adds the partner's copy, so lane slot j ends with the sums of
+                    // the steps u with u % LPC == j (same pairing as a butterfly)
+                    constexpr int kOut = kU / LPC;
+                    static_assert(kU % LPC == 0, "an ILP block holds whole lane groups");
 #pragma unroll
-                    for (int u = 0; u < kU; ++u) {
+                    for (int m = 1, cnt = kU; m < LPC; m <<= 1, cnt >>= 1) {
+                        const bool hi = (j & m) != 0;
 #pragma unroll
-                        for (int m = 1; m < LPC; m <<= 1)
-                            acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], m);
-                        if (u % LPC == j) part[(tb + u) * LY::kPartT + sc] = acc[u];
+                        for (int i = 0; i < cnt / 2; ++i) {
+                            const float keep = hi ? acc[2 * i + 1] : acc[2 * i];
+                            const float send = hi ? acc[2 * i] : acc[2 * i + 1];
+                            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                        }
                     }
+#pragma unroll
+                    for (int i = 0; i < kOut; ++i)
+                        part[(tb + i * LPC + j) * LY::kPartT + sc] = acc[i];
                 }
             }
         }
