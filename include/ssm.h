@@ -36,8 +36,9 @@
  *     delta_bias, the states and every intermediate are fp32.  bf16 outputs are
  *     rounded once, to nearest even.
  *   - y must not alias any input.  The decode state is updated in place by design.
- *   - Errors found on the device (a bounded wait that ran out) are written to a
- *     status word at the start of the workspace; read it with ssm_read_device_status.
+ *   - Errors found on the device (a bounded wait that ran out, or in a build with
+ *     SSM_DEBUG_BOUNDS=1 a failed index check) are written to a status word at the
+ *     start of the workspace; read it with ssm_read_device_status.
  *   - No C++ exception crosses this interface.
  */
 #ifndef SSM_B300_H
@@ -66,7 +67,9 @@ typedef enum {
     SSM_ERR_ALIGNMENT = 3,   /* a pointer is not aligned to its element size */
     SSM_ERR_WORKSPACE = 4,   /* workspace missing or smaller than *_workspace_size says */
     SSM_ERR_CUDA = 5,        /* the CUDA runtime reported an error at launch */
-    SSM_ERR_TIMEOUT = 6      /* (device status only) a bounded wait gave up */
+    SSM_ERR_TIMEOUT = 6,     /* (device status only) a bounded wait gave up */
+    SSM_ERR_BOUNDS = 7       /* (device status only, builds with SSM_DEBUG_BOUNDS=1) a
+                                kernel's index check failed; the access was skipped */
 } ssm_status;
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;

@@ -16,7 +16,7 @@ _lib = None
 SSM_F32, SSM_BF16 = 0, 1
 _STATUS = {0: "SSM_OK", 1: "SSM_ERR_INVALID_ARG", 2: "SSM_ERR_UNSUPPORTED",
            3: "SSM_ERR_ALIGNMENT", 4: "SSM_ERR_WORKSPACE", 5: "SSM_ERR_CUDA",
-           6: "SSM_ERR_TIMEOUT"}
+           6: "SSM_ERR_TIMEOUT", 7: "SSM_ERR_BOUNDS"}
 
 EXPORTED = ["ssm_scan_workspace_size", "ssm_scan_plan", "ssm_scan_fwd", "ssm_scan_fwd_noalloc",
             "ssm_scan_bwd_workspace_size", "ssm_scan_bwd",

@@ -122,4 +122,22 @@ __device__ __forceinline__ void report_status(DeviceStatus *st, int code, int wh
     }
 }
 
+// Index checks of the debug-bounds build (SSM_DEBUG_BOUNDS=1): the kernels guard their
+// global writes and TMA coordinates with in_bounds(...); a failed check records
+// SSM_ERR_BOUNDS with the site number in the status word and the caller skips the
+// access.  Release builds compile the checks out (in_bounds is true).
+#ifndef SSM_DEBUG_BOUNDS
+#define SSM_DEBUG_BOUNDS 0
+#endif
+constexpr bool kDebugBounds = SSM_DEBUG_BOUNDS != 0;
+__device__ __forceinline__ bool in_bounds(bool ok, DeviceStatus *st, int site) {
+    if constexpr (kDebugBounds) {
+        if (!ok) report_status(st, 7 /* SSM_ERR_BOUNDS */, site);
+        return ok;
+    } else {
+        (void)ok; (void)st; (void)site;
+        return true;
+    }
+}
+
 }  // namespace ssm

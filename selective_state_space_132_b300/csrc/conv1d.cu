@@ -239,7 +239,10 @@ __global__ void __launch_bounds__(kBlockT) conv1d_tma_kernel(const __grid_consta
             int d0, t0, b;
             coords(k0 + s, d0, t0, b);
             ptx::mbar_arrive_expect_tx(&bars[s], kTx);
-            ptx::tma_load_3d(smem + s * kStageB, &maps.x, &bars[s], d0, t0 - (K - 1), b);
+            // a debug-bounds build records a slab start off the 16-byte grid (and loads slab 0)
+            const int dc = in_bounds(d0 < D && (d0 * static_cast<int>(sizeof(TIO))) % 16 == 0 &&
+                                         b < p.batch && t0 < L, status, 141) ? d0 : 0;
+            ptx::tma_load_3d(smem + s * kStageB, &maps.x, &bars[s], dc, t0 - (K - 1), b);
         }
     }
     __syncthreads();
@@ -318,13 +321,17 @@ __global__ void __launch_bounds__(kBlockT) conv1d_tma_kernel(const __grid_consta
         ptx::fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
-            ptx::tma_store_3d(&maps.y, yb, d0, t0, b);
+            if (in_bounds(d0 < D && (d0 * static_cast<int>(sizeof(TIO))) % 16 == 0 && b < p.batch &&
+                              t0 >= 0 && t0 < L, status, 142))
+                ptx::tma_store_3d(&maps.y, yb, d0, t0, b);
             ptx::bulk_commit();
             if (k + kStagesT < k1) {
                 int nd0, nt0, nb;
                 coords(k + kStagesT, nd0, nt0, nb);
                 ptx::mbar_arrive_expect_tx(&bars[s], kTx);
-                ptx::tma_load_3d(smem + s * kStageB, &maps.x, &bars[s], nd0, nt0 - (K - 1), nb);
+                const int dc = in_bounds(nd0 < D && (nd0 * static_cast<int>(sizeof(TIO))) % 16 == 0 &&
+                                             nb < p.batch && nt0 < L, status, 141) ? nd0 : 0;
+                ptx::tma_load_3d(smem + s * kStageB, &maps.x, &bars[s], dc, nt0 - (K - 1), nb);
             }
         }
     }

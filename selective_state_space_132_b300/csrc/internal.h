@@ -108,6 +108,7 @@ struct ScanBwdParams {
     float *dA, *dB, *dC, *dD, *ddelta_bias, *dh0;
     float *ckpt;   // (B, ntiles, D, N) states at the tile starts
     int ckpt_given;  // 1: ckpt holds them already (written by the forward pass)
+    void *status;    // DeviceStatus at the start of the workspace
 };
 size_t scan_bwd_ckpt_floats(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate);
 // Steps between the backward pass's state checkpoints (its time tile): a power of two.

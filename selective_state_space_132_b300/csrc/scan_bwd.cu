@@ -155,6 +155,8 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c8 = lane >> 2, k = lane & 3;
+    DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
+    (void)status;
     const int c = warp * 8 + c8;                       // channel within the block
     const int64_t Dm = p.dim, L = p.seqlen, N = p.dstate;
     const int64_t b = blockIdx.y;
@@ -270,10 +272,12 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
     if (nt > 1 && !p.ckpt_given) prefetch(0, T, false);
     for (int64_t s = 0; s < nt && !p.ckpt_given; ++s) {
         float *ck = p.ckpt + ((b * nt + s) * Dm + d) * N + k * NS;
+        if (in_bounds(b < p.batch && s < nt, status, 151)) {
 #pragma unroll
-        for (int q = 0; q < NH; ++q) {
-            if (nval[2 * q]) ck[2 * q] = h[q].x;
-            if (nval[2 * q + 1]) ck[2 * q + 1] = h[q].y;
+            for (int q = 0; q < NH; ++q) {
+                if (nval[2 * q]) ck[2 * q] = h[q].x;
+                if (nval[2 * q + 1]) ck[2 * q + 1] = h[q].y;
+            }
         }
         if (s == nt - 1) break;                 // the last tile starts from this state
         __syncthreads();
@@ -457,6 +461,7 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
             if (!ccvalid) continue;
             const int e = t * kCB + cc;
             const int64_t i = (b * L + t0 + t) * Dm + dcc;
+            if (!in_bounds(t0 + t < L && b < p.batch, status, 152)) continue;
             const float gdl = sgdl[e];
             const float gdelta = p.softplus ? gdl * sigmoid_f(sv[e], kFast) : gdl;
             static_cast<TIO *>(p.dx)[i] = Io<TIO>::from_f(sgx[e]);
@@ -476,7 +481,8 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
             const float *src = sred + (t * 4 * 2 + kind) * NP + n;
             const float sum = src[0] + src[2 * NP] + src[4 * NP] + src[6 * NP];
             float *dst = kind ? p.dC : p.dB;
-            atomicAdd(dst + (b * L + t0 + t) * N + n, sum);
+            if (in_bounds(t0 + t < L && b < p.batch, status, 153))
+                atomicAdd(dst + (b * L + t0 + t) * N + n, sum);
         }
     }
     // ---- per-channel and per-state sums
@@ -485,7 +491,7 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int j = 2 * q + e;
-            if (!nval[j]) continue;
+            if (!nval[j] || !in_bounds(d < Dm && b < p.batch, status, 154)) continue;
             atomicAdd(p.dA + d * N + k * NS + j, e ? gA[q].y : gA[q].x);
             if (p.dh0) p.dh0[(b * Dm + d) * N + k * NS + j] = e ? lam[q].y : lam[q].x;
         }

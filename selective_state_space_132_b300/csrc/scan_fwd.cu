@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
     const int64_t D = p.dim, L = p.seqlen;
     const int N = static_cast<int>(p.dstate);
     const int K = p.nchunks;
+    DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
+    (void)status;
     const int b = blockIdx.y;
     const int c = blockIdx.z;
     const int d0 = blockIdx.x * kDT;
@@ -232,7 +234,8 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
                     // the state before step t0 + tq, at every checkpoint step (at least
                     // four steps apart, so only i = 0 can have one)
                     const int64_t t = t0 + tq + i;
-                    if (i == 0 && (tq & ((1 << p.ckpt_shift) - 1)) == 0 && dval && t < t_end) {
+                    if (i == 0 && (tq & ((1 << p.ckpt_shift) - 1)) == 0 && dval && t < t_end &&
+                        in_bounds((t >> p.ckpt_shift) < ck_tiles && b < p.batch, status, 111)) {
                         float *ck = p.ckpt + ((b * ck_tiles + (t >> p.ckpt_shift)) * D + d) * N;
 #pragma unroll
                         for (int k = 0; k < NS; ++k)
@@ -292,7 +295,7 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int64_t t = t0 + tq + i;
-                    if (pdval && t < t_end) {
+                    if (pdval && t < t_end && in_bounds(t < L && b < p.batch, status, 112)) {
                         float out = fmaf(pD, xv[i], av[i]);
                         if (has_z) out *= silu<kFast>(zv[i]);
                         gy[(static_cast<int64_t>(b) * L + t) * D + pdd] = Io<TIO>::from_f(out);
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
 
     if (kSummary) {
         const int64_t row = (static_cast<int64_t>(b) * K + c) * D + d;
-        if (dval) {
+        if (dval && in_bounds(row < p.batch * K * D && c < K - 1, status, 113)) {
 #pragma unroll
             for (int k = 0; k < NS; ++k) {
                 const int n = j * NS + k;
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(kDT * LPC, 512 / (kDT * LPC)) scan_kernel(Scan
             }
             if (j == 0) p.dsum[row] = dsum_acc;
         }
-    } else if (c == K - 1 && p.h_final && dval) {
+    } else if (c == K - 1 && p.h_final && dval && in_bounds(b < p.batch, status, 114)) {
 #pragma unroll
         for (int k = 0; k < NS; ++k) {
             const int n = j * NS + k;

@@ -249,12 +249,17 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
         const int s = tile % kStages;
         unsigned char *st = smem + s * LY::stage;
         const int t0 = static_cast<int>(t_begin + static_cast<int64_t>(tile) * kT);
+        // the channel coordinate must start a 16-byte row segment (else the copy faults):
+        // a debug-bounds build that finds one that does not records it and loads slab 0
+        const int dc = in_bounds(d0 >= 0 && d0 < D && (d0 * LY::E) % 16 == 0 && t0 >= 0 &&
+                                     t0 < L && b < p.batch, status, 101)
+                           ? d0 : 0;
         ptx::mbar_arrive_expect_tx(&bars[s], LY::tx_bytes(has_z));
-        ptx::tma_load_3d(st + LY::s_x, &maps.x, &bars[s], d0, t0, b);
-        ptx::tma_load_3d(st + LY::s_dl, &maps.dl, &bars[s], d0, t0, b);
+        ptx::tma_load_3d(st + LY::s_x, &maps.x, &bars[s], dc, t0, b);
+        ptx::tma_load_3d(st + LY::s_dl, &maps.dl, &bars[s], dc, t0, b);
         ptx::tma_load_3d(st + LY::s_B, &maps.B, &bars[s], 0, t0, b);
         if (!kSummary) {
-            if (has_z) ptx::tma_load_3d(st + LY::s_z, &maps.z, &bars[s], d0, t0, b);
+            if (has_z) ptx::tma_load_3d(st + LY::s_z, &maps.z, &bars[s], dc, t0, b);
             ptx::tma_load_3d(st + LY::s_C, &maps.C, &bars[s], 0, t0, b);
         }
     };
@@ -451,7 +456,8 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
                     // the state before step t0 + tb, at every checkpoint step (checkpoints
                     // are at least kU steps apart, so only a block's first step has one)
                     const int64_t t = t0 + tb;
-                    if ((tb & ((1 << p.ckpt_shift) - 1)) == 0 && sdval && t < t_end) {
+                    if ((tb & ((1 << p.ckpt_shift) - 1)) == 0 && sdval && t < t_end &&
+                        in_bounds((t >> p.ckpt_shift) < ck_tiles && b < p.batch, status, 102)) {
                         float2 *ck = reinterpret_cast<float2 *>(
                             p.ckpt + ((b * ck_tiles + (t >> p.ckpt_shift)) * D + sd) * N + j * NS);
 #pragma unroll
@@ -536,7 +542,8 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
         }
         __syncthreads();
         if (tid == 0) {
-            if (!kSummary) {
+            if (!kSummary && in_bounds(d0 >= 0 && d0 < D && (d0 * LY::E) % 16 == 0 && t0 >= 0 &&
+                                           t0 < L, status, 103)) {
                 ptx::tma_store_3d(&maps.y, smem + LY::o_y + (tile & 1) * align1k(LY::kTok), d0,
                                   static_cast<int>(t0), b);
                 ptx::bulk_commit();
@@ -560,7 +567,7 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
 
     if (kSummary) {
         const int64_t row = (static_cast<int64_t>(b) * K + c) * D + sd;
-        if (sdval) {
+        if (sdval && in_bounds(row < p.batch * K * D && c < K - 1, status, 104)) {
 #pragma unroll
             for (int k = 0; k < NS / 2; ++k) {
                 const int n = j * NS + 2 * k;
@@ -573,10 +580,11 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
             // publish: the block's summary writes happen before the flag's release
             __threadfence();
             __syncthreads();
-            if (tid == 0 && p.publish)
+            if (tid == 0 && p.publish &&
+                in_bounds(b < p.batch && c < K && slab < nslabs, status, 105))
                 ptx::st_release_u32(p.flags + (static_cast<int64_t>(b) * K + c) * nslabs + slab, 1u);
         }
-    } else if (c == K - 1 && p.h_final && sdval) {
+    } else if (c == K - 1 && p.h_final && sdval && in_bounds(b < p.batch, status, 106)) {
 #pragma unroll
         for (int k = 0; k < NS / 2; ++k) {
             const int n = j * NS + 2 * k;

@@ -222,7 +222,10 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
         const float *src;
         if (kind == 2) {
             int got = 1;
-            if (tid == 0) got = ptx::wait_flag(sk.flags + (k - 1), ptx::kWaitCycles) ? 1 : 0;
+            if (tid == 0)
+                got = in_bounds(k >= 1 && k - 1 < sk.nctas, status, 123) &&
+                              ptx::wait_flag(sk.flags + (k - 1), ptx::kWaitCycles)
+                          ? 1 : 0;
             if (__syncthreads_or(tid == 0 && !got)) {
                 ok = false;
                 pending = 3;
@@ -250,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
             //      L2 prefetch of the next one
             if (tid == 0) {
                 ptx::bulk_wait_read<0>();  // y store of the previous chunk has left sX
+                (void)in_bounds(g < p.ngroups && h < H && t0 < L && b < p.batch, status, 121);
                 ptx::mbar_arrive_expect_tx(bar_load, kLoadBytes);
                 for (int kb = 0; kb < 2; ++kb) {
                     ptx::tma_load_3d(sC + kb * kTile, &maps.C, bar_load, g * kN + 64 * kb, t0, b);
@@ -473,21 +477,22 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_tc_kernel(const __grid_consta
             ptx::tc_fence_before();
             __syncthreads();
             if (tid == 0) {
-                ptx::tma_store_3d(&maps.Y, sX, h * kP, t0, b);
+                if (in_bounds(h < H && t0 < L && b < p.batch, status, 122))
+                    ptx::tma_store_3d(&maps.Y, sX, h * kP, t0, b);
                 ptx::bulk_commit();
             }
         }
         if (!ok) break;
 
         // ---- the segment's final state: hand it over (head) or write h_final
-        if (kind == 1) {
+        if (kind == 1 && in_bounds(k < sk.nctas, status, 124)) {
             float *dst = sk.states + static_cast<int64_t>(k) * kP * kN;
 #pragma unroll
             for (int pp = 0; pp < kPH; ++pp) __stcg(dst + (kPH * hh + pp) * kN + row, S[pp]);
             __threadfence();
             __syncthreads();
             if (tid == 0) ptx::st_release_u32(sk.flags + k, 1u);
-        } else if (p.h_final) {
+        } else if (p.h_final && in_bounds(b < p.batch && h < H, status, 125)) {
             float *hf = p.h_final + (static_cast<int64_t>(b) * H + h) * kP * kN;
 #pragma unroll
             for (int pp = 0; pp < kPH; ++pp) hf[(kPH * hh + pp) * kN + row] = S[pp];

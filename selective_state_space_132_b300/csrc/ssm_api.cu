@@ -304,6 +304,7 @@ const char *ssm_status_string(ssm_status s) {
         case SSM_ERR_WORKSPACE: return "workspace missing or too small";
         case SSM_ERR_CUDA: return "CUDA runtime error";
         case SSM_ERR_TIMEOUT: return "a bounded device wait timed out";
+        case SSM_ERR_BOUNDS: return "a kernel index check failed (debug-bounds build)";
     }
     return "unknown status";
 }
@@ -634,6 +635,8 @@ ssm_status scan_bwd_impl(const ssm_scan_bwd_args *a, ssm_stream_t stream, const 
     p.ckpt = ckpt ? const_cast<float *>(ckpt)
                   : reinterpret_cast<float *>(static_cast<char *>(a->workspace) + ssm::kStatusBytes);
     p.ckpt_given = ckpt ? 1 : 0;
+    p.status = a->workspace;
+    if (cudaMemsetAsync(a->workspace, 0, ssm::kStatusBytes, st) != cudaSuccess) return SSM_ERR_CUDA;
     return from_cuda(ssm::launch_scan_bwd(p, st));
 }
 }  // namespace

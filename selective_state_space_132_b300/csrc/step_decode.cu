@@ -209,6 +209,13 @@ __global__ void __launch_bounds__(kTmaThreads, 5) decode_tma_kernel(DecodeParams
         uint64_t *bar = &bars[i % kTmaStages];
         const int r0 = tile_row(i);
         const uint32_t nr = tile_rows(i);
+        // bulk copies need 16-byte aligned, whole 16-byte spans inside the tensors; a
+        // debug-bounds build records a tile that breaks this and completes its stage empty
+        if (!in_bounds(r0 >= 0 && nr > 0 && nr <= static_cast<uint32_t>(R) && r0 + nr <= rows &&
+                           (r0 * TT::E) % 16 == 0 && (nr * TT::E) % 16 == 0, status, 131)) {
+            ptx::mbar_arrive_expect_tx(bar, 0);
+            return;
+        }
         ptx::mbar_arrive_expect_tx(bar, nr * (N * 4 + (kGate ? 3 : 2) * TT::E));
         bulk_load(st, p.state + static_cast<int64_t>(r0) * N, nr * N * 4, bar);
         bulk_load(st + TT::o_x, gx + r0, nr * TT::E, bar);
@@ -277,7 +284,8 @@ __global__ void __launch_bounds__(kTmaThreads, 5) decode_tma_kernel(DecodeParams
         ptx::fence_proxy_async_smem();  // the state written here is read by the bulk store
         __syncthreads();
         if (tid == 0) {
-            bulk_store(p.state + static_cast<int64_t>(tile_row(i)) * N, stg, tile_rows(i) * N * 4);
+            if (in_bounds(tile_row(i) + tile_rows(i) <= rows, status, 132))
+                bulk_store(p.state + static_cast<int64_t>(tile_row(i)) * N, stg, tile_rows(i) * N * 4);
             ptx::bulk_commit();
             if (i + kTmaStages < my) {
                 ptx::bulk_wait_read<0>();  // the stage's bytes have left shared memory
