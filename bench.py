@@ -696,7 +696,7 @@ def run_ours(args, world, rank, local):
         "config": bench_config(args.workload, p, world),
         # the scan is bound by instruction dispatch (ceilings: dispatch 669 us against
         # 331 us of HBM time at this workload), so the roofline is the ALU one; the HBM
-        # fraction the benchmark spec asks for sits beside it
+        # fraction sits beside it
         "roofline": {"bound": "alu", "achieved": rate, "peak": alu_peak,
                      "unit": "state-updates/s", "frac": rate / alu_peak, "traffic": traffic,
                      "peak_basis": f"{torch.cuda.get_device_properties(device).multi_processor_count}"

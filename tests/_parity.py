@@ -187,7 +187,7 @@ class Parity:
         with np.errstate(divide="ignore", invalid="ignore"):
             row_tol = row_tol + np.where(den_row > 0, np.sqrt(self.alw / den_row), 0.0)
         # a rel-L2 over fewer than 8 values is a per-element ratio; the element bound
-        # judges those rows (a one-value row of a sum with cancellation is no signal)
+        # covers those rows (a one-value row of a sum with cancellation is no signal)
         row_err = np.where(self.cnt >= 8, row_err, 0.0)
         worst = int(np.argmax(row_err / row_tol)) if self.nrows else 0
         atol = ATOL[io] * rms
