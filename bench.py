@@ -416,6 +416,14 @@ class L2Flush:
         torch.sum(self.r, dim=0, out=self.sink)
 
 
+def _gpu_lead():
+    """A short device-side spin (about 0.5 ms) queued before the start event of a timed
+    call that follows a synchronize: the host marshals the call and enqueues it while the
+    device spins, so the measured window holds the call's work and no host gap."""
+    import torch
+    torch.cuda._sleep(1_000_000)
+
+
 def _median_event_time(step, flush, iters):
     import torch
     for _ in range(3):
@@ -424,6 +432,7 @@ def _median_event_time(step, flush, iters):
     times = []
     for _ in range(iters):
         flush()
+        _gpu_lead()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         step()
@@ -482,6 +491,7 @@ def time_decode(p, steps, flush, device):
     flushed = []
     for i in range(min(steps, 50)):
         flush()
+        _gpu_lead()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         step(i)
@@ -523,6 +533,7 @@ def time_ssd_decode(nb, H, P, G, N, flush, device, iters=30):
     times = []
     for _ in range(iters):
         flush()
+        _gpu_lead()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         step()
