@@ -53,6 +53,20 @@ PROFILED_TRAFFIC = {
     },
 }
 
+# ncu occupancy of the binding resources of one scan launch, keyed like PROFILED_TRAFFIC:
+# dispatch_busy = (warp instructions + MUFU and packed-fp32 warp instructions, which take
+# two dispatch cycles) / (SM cycles x 4 sub-partitions x SMs); shared_wavefronts_of_peak =
+# l1tex__data_pipe_lsu_wavefronts_mem_shared.avg.pct_of_peak_sustained_elapsed
+# (profiles/scan_tma_bf16_B1_D2048_L131072_N16.md, "Shared memory and pipes")
+PROFILED_OCCUPANCY = {
+    "4271533a56edd623": {
+        "scan_bf16_B1_D2048_L131072_N16": {"dispatch_busy": 0.933, "shared_wavefronts_of_peak": 0.730,
+                                           "issue_active": 0.667},
+        "scan_bf16_B8_D1536_L2048_N16": {"dispatch_busy": 0.649, "shared_wavefronts_of_peak": 0.572,
+                                         "issue_active": 0.473},
+    },
+}
+
 WORKLOADS = {
     "scan_bf16_B8_D1536_L2048_N16": 1,
     "scan_bf16_B1_D2048_L131072_N16": 2,
@@ -718,6 +732,9 @@ def run_ours(args, world, rank, local):
                              "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
                              "algorithmic_bytes_per_launch": algo,
                              "frac_of_nominal_8000": achieved / 8000.0},
+                     # what the kernel's own binding units show under ncu (null once the
+                     # sources differ from the capture's)
+                     "profiled_occupancy": PROFILED_OCCUPANCY.get(src_hash, {}).get(args.workload),
                      "source_hash": src_hash},
         "gpu_launches": launches * args.steps,
         "wall_ms_per_step_incl_flush": wall / args.steps * 1e3,

@@ -37,6 +37,13 @@ def test_bench_prints_contract_line():
     h = r["hbm"]
     assert h["bound"] == "hbm" and h["unit"] == "GB/s" and 0 < h["frac"] < 1.5
     assert abs(h["frac"] - h["achieved"] / h["peak"]) < 1e-9
+    # ncu occupancy figures only for the sources they were captured on
+    occ = r["profiled_occupancy"]
+    import bench
+    if r["source_hash"] in bench.PROFILED_OCCUPANCY:
+        assert occ == bench.PROFILED_OCCUPANCY[r["source_hash"]].get(c["workload"])
+    else:
+        assert occ is None
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert "workload" in d["config"] and "l2" in d["config"]
