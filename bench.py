@@ -48,7 +48,7 @@ L2_FLUSH_BYTES = 256 << 20
 PROFILED_TRAFFIC = {
     "4271533a56edd623": {
         # scan_tma_lb_kernel (summary and output passes in one launch), mean of 5 calls:
-        # 2,974.9 MB read + 524.8 MB written (profiles/scan_tma_bf16_B1_D2048_L131072_N16.md)
+        # 2,974.9 MB read + 524.8 MB written (the launch list of the bench line's command)
         "scan_bf16_B1_D2048_L131072_N16": 3499700000,
     },
 }
@@ -56,8 +56,8 @@ PROFILED_TRAFFIC = {
 # ncu occupancy of the binding resources of one scan launch, keyed like PROFILED_TRAFFIC:
 # dispatch_busy = (warp instructions + MUFU and packed-fp32 warp instructions, which take
 # two dispatch cycles) / (SM cycles x 4 sub-partitions x SMs); shared_wavefronts_of_peak =
-# l1tex__data_pipe_lsu_wavefronts_mem_shared.avg.pct_of_peak_sustained_elapsed
-# (profiles/scan_tma_bf16_B1_D2048_L131072_N16.md, "Shared memory and pipes")
+# l1tex__data_pipe_lsu_wavefronts_mem_shared.avg.pct_of_peak_sustained_elapsed, one
+# captured launch per workload
 PROFILED_OCCUPANCY = {
     "4271533a56edd623": {
         "scan_bf16_B1_D2048_L131072_N16": {"dispatch_busy": 0.933, "shared_wavefronts_of_peak": 0.730,
