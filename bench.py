@@ -46,10 +46,10 @@ L2_FLUSH_BYTES = 256 << 20
 # kernel's sources at the time of the capture and by workload; an entry whose key no
 # longer matches the sources is ignored (traffic reported as null).
 PROFILED_TRAFFIC = {
-    "4271533a56edd623": {
+    "88390bb0d78ad0a6": {
         # scan_tma_lb_kernel (summary and output passes in one launch), mean of 5 calls:
-        # 2,974.9 MB read + 524.8 MB written (the launch list of the bench line's command)
-        "scan_bf16_B1_D2048_L131072_N16": 3499700000,
+        # 2,969.3 MB read + 525.3 MB written (the launch list of the bench line's command)
+        "scan_bf16_B1_D2048_L131072_N16": 3494627532,
     },
 }
 
@@ -59,11 +59,11 @@ PROFILED_TRAFFIC = {
 # l1tex__data_pipe_lsu_wavefronts_mem_shared.avg.pct_of_peak_sustained_elapsed, one
 # captured launch per workload
 PROFILED_OCCUPANCY = {
-    "4271533a56edd623": {
-        "scan_bf16_B1_D2048_L131072_N16": {"dispatch_busy": 0.933, "shared_wavefronts_of_peak": 0.730,
-                                           "issue_active": 0.667},
-        "scan_bf16_B8_D1536_L2048_N16": {"dispatch_busy": 0.649, "shared_wavefronts_of_peak": 0.572,
-                                         "issue_active": 0.473},
+    "88390bb0d78ad0a6": {
+        "scan_bf16_B1_D2048_L131072_N16": {"dispatch_busy": 0.935, "shared_wavefronts_of_peak": 0.731,
+                                           "issue_active": 0.668},
+        "scan_bf16_B8_D1536_L2048_N16": {"dispatch_busy": 0.685, "shared_wavefronts_of_peak": 0.588,
+                                         "issue_active": 0.501},
     },
 }
 

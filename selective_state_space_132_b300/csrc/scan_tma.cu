@@ -599,8 +599,7 @@ __device__ __forceinline__ bool chunk_pass(const TmaMaps &maps, const ScanParams
 // Two-launch form: the summary pass over chunks 0 .. K-2, then the output pass.
 template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kRed,
           bool kCkpt>
-__global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constant__ TmaMaps maps,
-                                                            ScanParams p) {
+__device__ __forceinline__ void scan_tma_entry(const TmaMaps &maps, const ScanParams &p) {
     using LY = Layout<TIO, NS, LPC, WPC, kSummary, kRed>;
     DeviceStatus *status = static_cast<DeviceStatus *>(p.status);
     // the first block of the first launch of a call clears the status word
@@ -609,6 +608,25 @@ __global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constan
         status->code = 0;
     (void)chunk_pass<TIO, NS, LPC, WPC, kSummary, kZoh, false, kRed, kCkpt>(
         maps, p, blockIdx.y, blockIdx.z, blockIdx.x * LY::CPB, blockIdx.x);
+}
+
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kRed,
+          bool kCkpt>
+__global__ void __launch_bounds__(32 * WPC) scan_tma_kernel(const __grid_constant__ TmaMaps maps,
+                                                            ScanParams p) {
+    scan_tma_entry<TIO, NS, LPC, WPC, kSummary, kZoh, kRed, kCkpt>(maps, p);
+}
+
+// The same pass under a register budget instead of launch bounds, for the bf16 Euler
+// output pass at four states per lane over four lanes: there the fully unrolled tile gets 72-80
+// registers and no spill, against 56 registers and a 16-byte spill under the launch
+// bounds (130M-layer shape: 191 against 198 us on B300).  Other instantiations spill
+// under the budget and keep the launch bounds.
+template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool kRed,
+          bool kCkpt>
+__global__ void __maxnreg__(96) scan_tma_kernel_r96(const __grid_constant__ TmaMaps maps,
+                                                    ScanParams p) {
+    scan_tma_entry<TIO, NS, LPC, WPC, kSummary, kZoh, kRed, kCkpt>(maps, p);
 }
 
 // Single-launch form with a decoupled look-back.  Blocks take their work from an atomic
@@ -646,7 +664,12 @@ template <typename TIO, int NS, int LPC, int WPC, bool kSummary, bool kZoh, bool
 cudaError_t launch_tma_one(const ScanParams &p, const TmaMaps &maps, int nchunks_grid,
                            cudaStream_t stream) {
     using LY = Layout<TIO, NS, LPC, WPC, kSummary, kRed>;
-    auto kern = scan_tma_kernel<TIO, NS, LPC, WPC, kSummary, kZoh, kRed, kCkpt>;
+    void (*kern)(const TmaMaps, ScanParams);
+    if constexpr (std::is_same<TIO, __nv_bfloat16>::value && NS == 4 && LPC == 4 && !kSummary &&
+                  !kZoh)
+        kern = scan_tma_kernel_r96<TIO, NS, LPC, WPC, kSummary, kZoh, kRed, kCkpt>;
+    else
+        kern = scan_tma_kernel<TIO, NS, LPC, WPC, kSummary, kZoh, kRed, kCkpt>;
     if (LY::bytes > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              LY::bytes);
