@@ -134,7 +134,7 @@ template <typename TIO> __device__ __forceinline__ float ld_io(const void *p, in
 }
 
 template <typename TIO, int NS, bool kZoh>
-__global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams p) {
+__device__ __forceinline__ void scan_bwd_body(const ScanBwdParams &p) {
     using S = BwdShape<NS>;
     constexpr int NP = S::NP, T = S::T;
     constexpr bool kFast = std::is_same<TIO, __nv_bfloat16>::value;
@@ -513,9 +513,28 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams 
 }
 
 template <typename TIO, int NS, bool kZoh>
+__global__ void __launch_bounds__(kThreads) scan_bwd_kernel(const ScanBwdParams p) {
+    scan_bwd_body<TIO, NS, kZoh>(p);
+}
+
+// Up to four states per lane the kernel runs under a register budget instead of launch
+// bounds: 168 registers is the most that keeps three 128-thread blocks per SM, and the
+// compiler then schedules the unrolled loops without spills (96 registers under launch
+// bounds at the 130M-layer shape; 1072 -> 1018 us, 938 -> 880 us from forward
+// checkpoints, on B300).  More states per lane spill under the budget.
+template <typename TIO, int NS, bool kZoh>
+__global__ void __maxnreg__(168) scan_bwd_kernel_r168(const ScanBwdParams p) {
+    scan_bwd_body<TIO, NS, kZoh>(p);
+}
+
+template <typename TIO, int NS, bool kZoh>
 cudaError_t launch_ns(const ScanBwdParams &p, cudaStream_t stream) {
     using S = BwdShape<NS>;
-    auto kern = scan_bwd_kernel<TIO, NS, kZoh>;
+    void (*kern)(const ScanBwdParams);
+    if constexpr (NS <= 4)
+        kern = scan_bwd_kernel_r168<TIO, NS, kZoh>;
+    else
+        kern = scan_bwd_kernel<TIO, NS, kZoh>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(S::bytes));
     if (e != cudaSuccess) return e;
